@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Throughput of the S5 layer forward hot path on GB300.
+
+One step = zero-order-hold discretisation (s5_discretize) + the fused forward
+(s5_forward: projection, chunked scan with decoupled look-back, readout) over
+one batch of the long-sequence workload (B=8, L=16384, H=128, P=128, bf16
+u/y; the Path-X sequence length), with inputs resident in HBM.  Four
+input/output sets (4 x 67 MB > 129 MB L2) rotate between steps so that every
+step reads u from HBM.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the float64 CPU
+oracle on the same workload instead (bounded sample per step).
+
+Multi-GPU: replicas only.  Each rank runs an independent copy of the
+workload (sequences are independent; the layer needs no exchange), the timed
+region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "S5 layer fwd tokens/s (batch*L/s) and fraction of HBM/tensor roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="pathx_bf16",
+                    choices=["small", "fp32", "pathx_bf16", "irregular"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk.get("bf16_tflops", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch):
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def traffic_for(kernel: str, source: str):
+    """ncu DRAM bytes per launch recorded for this kernel, if its source is
+    unchanged since the capture (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+        sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
+        if rec and rec.get("source_sha256") == sha:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(w, u_bytes_per, y_bytes_per):
+    params = 8 * w.P + 8 * w.P * w.H * 2 + 4 * w.H
+    if w.varying_dt:
+        params += 4 * w.P + 4 * w.B * w.L      # log_dt and the gaps
+    return w.B * w.L * w.H * (u_bytes_per + y_bytes_per) + params
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from diagonal_state_space_gb300 import api
+    from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    u_dt = torch.bfloat16 if w.u_dtype == "bf16" else torch.float32
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    lam, log_dt = dev(inp["lambda_"]), dev(inp["log_dt"])
+    bt, ct, d = dev(inp["b_tilde"]), dev(inp["c_tilde"]), dev(inp["d"])
+    g = dev(inp["g"]) if w.varying_dt else None
+    NSETS = 4
+    u_sets = [dev(inp["u"]).to(u_dt) for _ in range(NSETS)]
+    y_sets = [torch.empty_like(u_sets[0]) for _ in range(NSETS)]
+    lb = torch.empty(w.P, dtype=torch.complex64, device="cuda")
+    bb = torch.empty(w.P, w.H, dtype=torch.complex64, device="cuda")
+    ws = api.new_workspace(w.B, w.L, w.H, w.P)
+    stream = torch.cuda.current_stream()
+
+    fwd_ev = []
+
+    def step(i, timed):
+        u, y = u_sets[i % NSETS], y_sets[i % NSETS]
+        if w.varying_dt:
+            if timed:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            api.s5_forward_varying_dt(lam, log_dt, bt, ct, d, g, u, y=y, proj_dtype=w.proj_dtype,
+                                      workspace=ws)
+        else:
+            api.s5_discretize(lam, log_dt, bt, lb, bb)
+            if timed:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            api.s5_forward(lb, bb, ct, d, u, y=y, proj_dtype=w.proj_dtype, workspace=ws)
+        if timed:
+            e1.record(stream)
+            fwd_ev.append((e0, e1))
+
+    for i in range(max(3, args.warmup)):
+        step(i, False)
+    torch.cuda.synchronize()
+    st = api.s5_sync_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = t_start.elapsed_time(t_end)
+    if dist:
+        tt = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    st = api.s5_sync_status(ws)
+    if st != 0:
+        raise RuntimeError("device status %d after the timed region" % st)
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    fwd_avg_s = statistics.fmean(fwd_ms) / 1e3
+    ms_step = ms_total / args.steps
+    tokens = w.B * w.L
+    value = tokens * world / (ms_step / 1e3)
+
+    # end-to-end through the public API with host buffers
+    u_host = torch.from_numpy(np.ascontiguousarray(inp["u"])).to(u_dt).pin_memory()
+    y_host = torch.empty(u_host.shape, dtype=u_dt).pin_memory()
+    host_params = [torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+                   for k in ("lambda_", "log_dt", "b_tilde", "c_tilde", "d")]
+    if w.varying_dt:
+        host_params.append(torch.from_numpy(np.ascontiguousarray(inp["g"])).pin_memory())
+    dev_params = [torch.empty_like(p, device="cuda") for p in host_params]
+    u_dev, y_dev = u_sets[0], y_sets[0]
+
+    def e2e_step():
+        u_dev.copy_(u_host, non_blocking=True)
+        for hp, dp in zip(host_params, dev_params):
+            dp.copy_(hp, non_blocking=True)
+        if w.varying_dt:
+            api.s5_forward_varying_dt(*dev_params[:5], dev_params[5], u_dev, y=y_dev,
+                                      proj_dtype=w.proj_dtype, workspace=ws)
+        else:
+            l_, b_ = api.s5_discretize(dev_params[0], dev_params[1], dev_params[2], lb, bb)
+            api.s5_forward(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
+                           proj_dtype=w.proj_dtype, workspace=ws)
+        y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = u_host.numel() * u_host.element_size() + sum(p.numel() * p.element_size()
+                                                       for p in host_params)
+    d2h = y_host.numel() * y_host.element_size()
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return None
+
+    hbm_gbs, _, peak_kind = load_peaks()
+    ub = 2 if w.u_dtype == "bf16" else 4
+    alg = algorithmic_bytes(w, ub, ub)
+    achieved = alg / fwd_avg_s / 1e9
+    kname = "fwd_simt_kernel"
+    src = os.path.join(ROOT, "diagonal_state_space_gb300", "csrc", "s5_forward_simt.cu")
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64: u~N(0,1), lambda=-1/2+i*pi*n, "
+                "log_dt~U[ln1e-3,ln1e-1], B~,C~~CN(0,1/H), D~N(0,1))",
+        "config": {
+            "workload": "%s: S5 layer forward, B=%d L=%d H=%d P=%d (stored complex modes), "
+                        "u/y %s, proj %s, complex fp32 scan%s" % (
+                            w.name, w.B, w.L, w.H, w.P, w.u_dtype, w.proj_dtype,
+                            ", per-step interval" if w.varying_dt else ""),
+            "global_batch": w.B * world, "seq_len": w.L, "H": w.H, "P": w.P,
+            "step": ("s5_forward_varying_dt" if w.varying_dt else "s5_discretize + s5_forward"),
+            "l2": "4 rotating input/output sets (%.0f MB > 129 MB L2)" % (
+                NSETS * tokens * w.H * 2 * ub / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": kname,
+            "achieved": achieved,
+            "peak": hbm_gbs,
+            "unit": "GB/s",
+            "frac": achieved / hbm_gbs,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                           if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": alg,
+            "launch_us": fwd_avg_s * 1e6,
+            "traffic": traffic_for(kname, src),
+        },
+        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (2 if not w.varying_dt else 2),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+# ---------------------------------------------------------------------------
+def oracle_run(w, inp, seqs):
+    import oracle
+    if w.varying_dt:
+        return oracle.forward_varying_dt(inp["lambda_"], inp["log_dt"], inp["b_tilde"],
+                                         inp["c_tilde"], inp["d"], inp["g"][seqs], inp["u"][seqs])
+    lb, bb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    return oracle.forward(lb, bb, inp["c_tilde"], inp["d"], inp["u"][seqs])
+
+
+def cpu_baseline(w, inp):
+    """The float64 oracle, as it stands, single-threaded on one host core."""
+    seqs = list(range(w.B))
+    t0 = time.perf_counter()
+    oracle_run(w, inp, seqs)
+    dt = time.perf_counter() - t0
+    return {"value": len(seqs) * w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "the whole workload (%d sequences x %d tokens), one pass, %.1f s"
+                      % (len(seqs), w.L, dt),
+            "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    steps = max(1, min(args.steps, 10))
+    warm = max(1, min(args.warmup, 2))
+    seqs = [0]          # one sequence per step keeps the run to a few minutes
+    for _ in range(warm):
+        oracle_run(w, inp, seqs)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_run(w, inp, seqs)
+    dt = (time.perf_counter() - t0) / steps
+    v = len(seqs) * w.L / dt
+    sample = "%d sequence x %d tokens per step (of %d sequences)" % (len(seqs), w.L, w.B)
+    res = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+           "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P,
+                      "reference": "float64 CPU oracle (oracle/s5_oracle.c), single thread"},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return res
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

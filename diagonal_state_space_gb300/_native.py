@@ -1,0 +1,63 @@
+"""ctypes loader of libs5.so.  Loading fails loudly: there is no fallback."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libs5.so")
+
+S5_F32, S5_BF16 = 0, 1
+STATUS = {0: "S5_OK", 1: "S5_ERR_INVALID_ARGUMENT", 2: "S5_ERR_UNSUPPORTED", 3: "S5_ERR_CUDA",
+          4: "S5_ERR_TIMEOUT", 5: "S5_ERR_NONFINITE"}
+
+# Every exported entry point of include/s5.h: name -> (restype, argtypes)
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "s5_discretize": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "s5_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                        _vp, _sz, _vp]),
+    "s5_forward_varying_dt": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
+                                   _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "s5_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "s5_sync_status": (_i, [_vp, _vp]),
+    "s5_status_string": (ctypes.c_char_p, [_i]),
+    "s5_last_cuda_error": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class S5Error(RuntimeError):
+    def __init__(self, fn: str, code: int, detail: str = ""):
+        self.code = code
+        msg = "%s failed: %s" % (fn, STATUS.get(code, str(code)))
+        if detail:
+            msg += " (%s)" % detail
+        super().__init__(msg)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libs5.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libs5.so is not built (%s); run __graft_entry__.build() or "
+                                   "python diagonal_state_space_gb300/build.py" % LIB_PATH)
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(h, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = h
+    return _lib
+
+
+def check(fn: str, code: int) -> None:
+    if code != 0:
+        detail = ""
+        if code == 3:
+            detail = lib().s5_last_cuda_error().decode()
+        raise S5Error(fn, code, detail)

@@ -29,9 +29,9 @@ import numpy as np
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bfloat16 (ties to even); returns float32."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    rnd = ((bits >> 16) & 1) + 0x7FFF
-    out = (((bits + rnd) >> 16) << 16).astype(np.uint32)
+    bits = x.view(np.uint32)
+    # finite values: bits + 0x8000 stays below 2^32, so uint32 arithmetic is exact
+    out = (bits + (((bits >> 16) & 1) + 0x7FFF)) & np.uint32(0xFFFF0000)
     return out.view(np.float32).reshape(x.shape)
 
 
