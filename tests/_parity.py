@@ -8,8 +8,10 @@ from diagonal_state_space_gb300 import api
 
 
 def rel_l2(got, ref):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
+    cplx = np.iscomplexobj(got) or np.iscomplexobj(ref)
+    dt = np.complex128 if cplx else np.float64
+    got = np.asarray(got, dt)
+    ref = np.asarray(ref, dt)
     den = np.linalg.norm(ref)
     return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
 
