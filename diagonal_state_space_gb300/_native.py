@@ -8,6 +8,7 @@ import threading
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libs5.so")
 
 S5_F32, S5_BF16 = 0, 1
+S5_NOALLOC_SCRATCH_BYTES = 8 << 20   # include/s5.h
 STATUS = {0: "S5_OK", 1: "S5_ERR_INVALID_ARGUMENT", 2: "S5_ERR_UNSUPPORTED", 3: "S5_ERR_CUDA",
           4: "S5_ERR_TIMEOUT", 5: "S5_ERR_NONFINITE"}
 
@@ -19,6 +20,8 @@ SIGNATURES = {
                         _vp, _sz, _vp]),
     "s5_forward_varying_dt": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
                                    _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "s5_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                                _vp, _vp]),
     "s5_workspace_size": (_sz, [_i, _i, _i, _i]),
     "s5_sync_status": (_i, [_vp, _vp]),
     "s5_status_string": (ctypes.c_char_p, [_i]),

@@ -120,11 +120,37 @@ def s5_forward_varying_dt(lam, log_dt, b_tilde, c_tilde, d, dt_scale, u, y=None,
     return y if x_last is None else (y, x_last)
 
 
+def s5_forward_noalloc(lambda_bar, b_bar, c_tilde, d, u, y, proj_dtype="f32", x0=None,
+                       x_last=None, stream=None):
+    """s5_forward for callers that cannot allocate device memory: no workspace,
+    and no tensor is created here either (y, and x_last if wanted, are the
+    caller's).  The library keeps the carry scratch in a fixed device array of
+    S5_NOALLOC_SCRATCH_BYTES; larger problems are rejected.  Calls that overlap
+    on the GPU share that array and race, so serialize them."""
+    P = b_bar.shape[0]
+    Bn, L, H = u.shape
+    need = s5_workspace_size(Bn, L, H, P)
+    if need > _native.S5_NOALLOC_SCRATCH_BYTES:
+        raise S5Error("s5_forward_noalloc", 1,
+                      "needs %d bytes of carry scratch, more than the library's fixed %d"
+                      % (need, _native.S5_NOALLOC_SCRATCH_BYTES))
+    c64 = torch.complex64
+    code = _native.lib().s5_forward_noalloc(
+        _ptr(lambda_bar, "lambda_bar", c64, (P,)), _ptr(b_bar, "b_bar", c64, (P, H)),
+        _ptr(c_tilde, "c_tilde", c64, (H, P)), _ptr(d, "d", torch.float32, (H,)),
+        _ptr(u, "u"), _DT[u.dtype], _ptr(y, "y", None, (Bn, L, H)), _DT[y.dtype],
+        _DT_NAME[proj_dtype], Bn, L, H, P, _ptr(x0, "x0", c64, (Bn, P), True),
+        _ptr(x_last, "x_last", c64, (Bn, P), True), _stream(stream))
+    check("s5_forward_noalloc", code)
+    return y if x_last is None else (y, x_last)
+
+
 def s5_sync_status(workspace, stream=None) -> int:
     """Waits for the stream; returns and clears the latched device status."""
     return int(_native.lib().s5_sync_status(_ptr(workspace, "workspace", torch.uint8),
                                             _stream(stream)))
 
 
-__all__ = ["s5_discretize", "s5_forward", "s5_forward_varying_dt", "s5_workspace_size",
+__all__ = ["s5_discretize", "s5_forward", "s5_forward_varying_dt", "s5_forward_noalloc",
+           "s5_workspace_size",
            "s5_sync_status", "new_workspace", "S5Error", "S5_F32", "S5_BF16"]

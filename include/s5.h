@@ -118,6 +118,33 @@ s5_status s5_forward_varying_dt(const float *lambda, const float *log_dt, const 
  * small header).  Returns 0 for invalid sizes. */
 size_t s5_workspace_size(int B, int L, int H, int P);
 
+/*
+ * s5_forward without a workspace, for callers that cannot allocate device
+ * memory (a plugin in a host application that owns all device memory, a
+ * latency-critical loop that must not enter the allocator, an embedded
+ * deployment with a fixed memory budget).  The paper has no counterpart.
+ * Arguments, layouts and results are those of s5_forward; the caller still
+ * passes every input and output.  The carry scratch is a fixed device array
+ * of S5_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
+ * it until the process exits.
+ *  - Sizes whose s5_workspace_size(B,L,H,P) exceeds S5_NOALLOC_SCRATCH_BYTES
+ *    are rejected with S5_ERR_INVALID_ARGUMENT before anything is queued.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *    library routine.  It clears the scratch's header and flags on `stream`
+ *    (cudaMemsetAsync) and launches the CUDA-core forward kernel.
+ *  - Every call shares the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race and give wrong results.  Serialize them.
+ *  - Device-side conditions (a carry wait that gave up) are not reported.
+ */
+#define S5_NOALLOC_SCRATCH_BYTES (8u << 20)
+s5_status s5_forward_noalloc(const float *lambda_bar, const float *b_bar, const float *c_tilde,
+                             const float *d, const void *u, s5_dtype u_dtype, void *y,
+                             s5_dtype y_dtype, s5_dtype proj_dtype, int B, int L, int H, int P,
+                             const float *x0, float *x_last, s5_stream_t stream);
+
 /* Waits for `stream`, returns the first device-side condition latched in
  * `workspace` since the last call (S5_OK if none) and clears it. */
 s5_status s5_sync_status(void *workspace, s5_stream_t stream);
