@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "s5_simt.cuh"
+#include "s5_tc.cuh"
 
 namespace s5 {
 cudaError_t launch_discretize(const float2 *, const float *, const float2 *, int, int, float2 *,
@@ -48,9 +49,10 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 int min_tile_tokens(int H, int P) {
     int t0 = s5::simt_tile_tokens(H, P, false);
     int t1 = s5::simt_tile_tokens(H, P, true);
-    if (t0 == 0) return t1;
-    if (t1 == 0) return t0;
-    return t0 < t1 ? t0 : t1;
+    int t = t0 == 0 ? t1 : (t1 == 0 ? t0 : (t0 < t1 ? t0 : t1));
+    if (s5::tc_supported(H, P, true, true, true) && (t == 0 || s5::TC_TILE_TOKENS < t))
+        t = s5::TC_TILE_TOKENS;
+    return t;
 }
 
 // Shared checks of the two forward entry points.
@@ -115,6 +117,32 @@ s5_status run_simt(const float2 *lambda_bar, const float2 *w, const float2 *c_ti
     return e == cudaSuccess ? S5_OK : cuda_fail(e);
 }
 
+// Tensor-core path: bf16 operands, fp32 accumulation, complex fp32 scan.
+s5_status run_tc(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_tilde,
+                 const float *d, const void *u, void *y, int B, int L, int H, int P,
+                 const float *x0, float *x_last, void *workspace, cudaStream_t st) {
+    const int sms = num_sms_current();
+    if (sms == 0) return cuda_fail(cudaGetLastError());
+    const long long nchunks = ceil_div(L, s5::TC_TILE_TOKENS);
+    const long long ntiles = nchunks * B;
+    if (ntiles >= (1ll << 31)) return S5_ERR_UNSUPPORTED;
+    s5::TcArgs a;
+    a.lambda_bar = lambda_bar;
+    a.b_bar = b_bar;
+    a.c_tilde = c_tilde;
+    a.d = d;
+    a.x0 = reinterpret_cast<const float2 *>(x0);
+    a.x_last = reinterpret_cast<float2 *>(x_last);
+    a.B = B;
+    a.L = L;
+    a.nchunks = (int)nchunks;
+    a.ntiles = (int)ntiles;
+    a.ws = s5::ws_layout(workspace, ntiles, P);
+    (void)H;
+    cudaError_t e = s5::launch_forward_tc(a, u, y, st, sms);
+    return e == cudaSuccess ? S5_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,6 +193,11 @@ s5_status s5_forward(const float *lambda_bar, const float *b_bar, const float *c
                                 x_last, workspace, workspace_bytes);
     if (s != S5_OK) return s;
     if ((long long)B * L == 0) return empty_forward(B, P, x0, x_last, st);
+    if (s5::tc_supported(H, P, u_dtype == S5_BF16, y_dtype == S5_BF16, proj_dtype == S5_BF16))
+        return run_tc(reinterpret_cast<const float2 *>(lambda_bar),
+                      reinterpret_cast<const float2 *>(b_bar),
+                      reinterpret_cast<const float2 *>(c_tilde), d, u, y, B, L, H, P, x0, x_last,
+                      workspace, st);
     return run_simt(reinterpret_cast<const float2 *>(lambda_bar),
                     reinterpret_cast<const float2 *>(b_bar),
                     reinterpret_cast<const float2 *>(c_tilde), d, nullptr, u, u_dtype, y, y_dtype,

@@ -1,0 +1,25 @@
+// s5_tc.cuh -- arguments of the tensor-core forward kernel (s5_forward_tc.cu).
+#pragma once
+#include "s5_internal.cuh"
+
+namespace s5 {
+
+constexpr int TC_TILE_TOKENS = 64;
+
+struct TcArgs {
+    const float2 *lambda_bar;  // [P]
+    const float2 *b_bar;       // [P][H]
+    const float2 *c_tilde;     // [H][P]
+    const float *d;            // [H]
+    const float2 *x0;          // [B][P] or null
+    float2 *x_last;            // [B][P] or null
+    int B, L, nchunks, ntiles;
+    WsLayout ws;               // per-mode carry records live in ws.agg
+};
+
+// The tensor-core kernel covers H = 128, P = 128 with bf16 u, y and projections.
+bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16);
+cudaError_t launch_forward_tc(const TcArgs &a, const void *u, void *y, cudaStream_t st,
+                              int num_sms);
+
+}  // namespace s5

@@ -1,0 +1,82 @@
+"""GPU parity of the tensor-core forward (H = 128, P = 128, bf16 u/y and
+projections, complex fp32 scan) against the float64 oracle.  Bar: relative L2
+error <= 2e-2 per output tensor (bf16-projection path)."""
+import numpy as np
+import pytest
+import torch
+
+from diagonal_state_space_gb300 import api
+from diagonal_state_space_gb300.workloads import make_layer_inputs
+
+from _parity import dev, host, layer_to_device, oracle_forward, rel_l2
+
+pytestmark = pytest.mark.gpu
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _run(B, L, seed, zero_d=False, x0=None):
+    inp = make_layer_inputs(B, L, 128, 128, seed=seed, u_dtype="bf16")
+    if zero_d:
+        inp["d"] = np.zeros_like(inp["d"])
+    t = layer_to_device(inp, "bf16")
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    x0d = None if x0 is None else dev(x0)
+    y, xl = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16", x0=x0d,
+                           x_last=True)
+    assert y.dtype == torch.bfloat16
+    oy, oxl = oracle_forward(inp, x0=x0)
+    return host(y), oy, host(xl), oxl
+
+
+@pytest.mark.parametrize("B,L", [(1, 64), (1, 1), (1, 63), (1, 65), (2, 128), (3, 1000),
+                                 (8, 4097), (1, 20000)])
+@pytest.mark.parametrize("zero_d", [False, True])
+def test_tc_forward_matches_oracle(B, L, zero_d):
+    y, oy, xl, oxl = _run(B, L, seed=31 * B + L, zero_d=zero_d)
+    assert rel_l2(y, oy) <= BF16_TOL
+    assert rel_l2(xl, oxl) <= BF16_TOL
+
+
+def test_tc_forward_with_initial_state():
+    rng = np.random.default_rng(5)
+    x0 = (rng.standard_normal((4, 128)) + 1j * rng.standard_normal((4, 128))).astype(np.complex64)
+    y, oy, xl, oxl = _run(4, 777, seed=12, zero_d=True, x0=x0)
+    assert rel_l2(y, oy) <= BF16_TOL
+    assert rel_l2(xl, oxl) <= BF16_TOL
+
+
+def test_tc_repeat_calls_share_a_workspace():
+    inp = make_layer_inputs(8, 2048, 128, 128, seed=3, u_dtype="bf16")
+    t = layer_to_device(inp, "bf16")
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    ws = api.new_workspace(8, 2048, 128, 128)
+    outs = [host(api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16",
+                                workspace=ws)) for _ in range(3)]
+    assert api.s5_sync_status(ws) == 0
+    oy, _ = oracle_forward(inp)
+    for o in outs:
+        assert rel_l2(o, oy) <= BF16_TOL
+    assert rel_l2(outs[1], outs[2]) <= 1e-3
+
+
+def test_tc_carry_wait_timeout_is_reported_and_recoverable():
+    inp = make_layer_inputs(1, 1024, 128, 128, seed=4, u_dtype="bf16")
+    t = layer_to_device(inp, "bf16")
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    ws = api.new_workspace(1, 1024, 128, 128)
+    words = ws.view(torch.int32)
+    words[4] = 1          # tile 0 never publishes its carry record
+    words[5] = 2000       # 2 ms wait limit
+    api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16", workspace=ws)
+    assert api.s5_sync_status(ws) == 4
+    words[4] = 0
+    words[5] = 0
+    y = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16", workspace=ws)
+    assert api.s5_sync_status(ws) == 0
+    assert rel_l2(host(y), oracle_forward(inp)[0]) <= BF16_TOL
