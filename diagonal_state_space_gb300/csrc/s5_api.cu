@@ -166,7 +166,7 @@ size_t s5_workspace_size(int B, int L, int H, int P) {
     const int T = min_tile_tokens(H, P);
     if (T == 0) return 0;
     const long long ntiles = (long long)B * ceil_div(L, T);
-    return s5::ws_bytes(ntiles, P);
+    return s5::ws_bytes(ntiles, P, H);
 }
 
 s5_status s5_discretize(const float *lambda, const float *log_dt, const float *b_tilde, int P,

@@ -4,19 +4,23 @@
 // 1, 3, 4; summary "SIMPLIFIED STATE SPACE LAYERS ...", App. A and App. H):
 //   Bu_k = B_bar u_k,  x_k = lambda_bar * x_{k-1} + Bu_k,  y_k = 2 Re(C~ x_k) + D u_k.
 //
-// One persistent CTA per SM claims tiles of 64 tokens of one sequence, in
-// order, and runs a warp-specialised pipeline over them:
-//   warp 0      TMA: u tile [64 tokens x 128 features] bf16 -> smem (3 stages)
-//   warp 1      tcgen05.mma issuer:
-//                 GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T        (into TMEM)
-//                 GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T        (into TMEM)
-//   warp 2      TMEM allocation (512 columns: 4 regions of 128)
-//   warps 4-7   scan: thread = mode (= TMEM lane); pass 1 folds the tile's
-//               64 steps from zero, publishes the aggregate, decoupled
-//               look-back for the carry, pass 2 reruns from the carry and
-//               writes x_k as bf16 into the GEMM2 operand X [64 x 2P]
-//   warps 8-11  epilogue: thread = feature (= TMEM lane of GEMM2);
-//               y = D2 + D*u, written over u in the stage, TMA store.
+// A prep kernel writes the bf16 operand images of B_bar and C' into the
+// workspace.  Then one persistent CTA per SM claims tiles of 64 tokens of one
+// sequence, in order, and runs a warp-specialised pipeline over them:
+//   warp 0        TMA: u tile [64 tokens x 128 features] bf16 -> smem (3 stages);
+//                 bulk copy of the two weight images at start-up
+//   warp 1        tcgen05.mma issuer, driven by whichever input is ready:
+//                   GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T      (into TMEM)
+//                   GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T      (into TMEM)
+//   warp 2        TMEM allocation (512 columns: 4 regions of 128)
+//   warps 4-7     scan group 0 (even local tiles) } thread = mode = TMEM lane:
+//   warps 8-11    scan group 1 (odd local tiles)  } pass 1 folds the tile's 64
+//                 steps from zero, publishes the aggregate, decoupled look-back
+//                 for the carry, pass 2 reruns from the carry and writes x_k as
+//                 bf16 into the GEMM2 operand X [64 x 2P].  Two groups let one
+//                 group's look-back overlap the other group's passes.
+//   warps 12-15   epilogue: thread = feature = TMEM lane of GEMM2;
+//                 y = D2 + D*u, written over u in the stage, TMA store.
 // Bs holds B_bar split into real rows (0..P-1) and imaginary rows (P..2P-1);
 // C' interleaves (2 Re C~, -2 Im C~) so that K = 2P of GEMM2 pairs with X's
 // interleaved (Re x, Im x): sum_k C'[h][k] X[t][k] = 2 Re(C~ x_t)[h].
@@ -41,18 +45,21 @@ constexpr int H_F = 128;                // features
 constexpr int P_M = 128;                // stored complex modes
 constexpr int STAGES = 3;
 constexpr int REGIONS = 4;              // TMEM regions of 128 columns
-constexpr int THREADS = 384;
-constexpr int W_PROD = 0, W_MMA = 1, W_TMEM = 2, W_SCAN = 4, W_EPI = 8;
+constexpr int THREADS = 512;
+constexpr int W_PROD = 0, W_MMA = 1, W_TMEM = 2, W_SCAN = 4, W_EPI = 12;
 
-constexpr uint32_t SM_BS = 0;                          // [2 kb][2P rows][128 B]
-constexpr uint32_t SM_CP = SM_BS + 2 * 2 * P_M * 128;  // [4 kb][H rows][128 B]
-constexpr uint32_t SM_U = SM_CP + 4 * H_F * 128;       // [stage][2 kb][64 rows][128 B]
+constexpr uint32_t BS_BYTES = 2 * 2 * P_M * 128;       // [2 kb][2P rows][128 B]
+constexpr uint32_t CP_BYTES = 4 * H_F * 128;           // [4 kb][H rows][128 B]
+constexpr uint32_t SM_BS = 0;
+constexpr uint32_t SM_CP = SM_BS + BS_BYTES;
+constexpr uint32_t SM_U = SM_CP + CP_BYTES;            // [stage][2 kb][64 rows][128 B]
 constexpr uint32_t U_STAGE = 2 * T_TOK * 128;
 constexpr uint32_t SM_X = SM_U + STAGES * U_STAGE;     // [4 kb][64 rows][128 B]
 constexpr uint32_t SM_BAR = SM_X + 4 * T_TOK * 128;
 constexpr uint32_t SM_TOTAL = SM_BAR + 512;
 constexpr uint32_t SMEM_REQUEST = SM_TOTAL + 1024;     // slack for 1024-B alignment
 static_assert(SMEM_REQUEST <= 227 * 1024, "shared memory budget");
+static_assert(BS_BYTES + CP_BYTES == 8 * P_M * H_F, "image size");
 
 constexpr unsigned long long PIPE_WAIT_NS = 2000000000ull;   // 2 s per pipeline wait
 constexpr unsigned long long DRAIN_WAIT_NS = 200000000ull;   // 0.2 s per teardown wait
@@ -60,23 +67,31 @@ constexpr unsigned long long DRAIN_WAIT_NS = 200000000ull;   // 0.2 s per teardo
 struct Bars {
     uint64_t full_u[STAGES], empty_u[STAGES];
     uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], mma2_done[REGIONS];
-    uint64_t xready, xfree, drain;
+    uint64_t xready, xfree[2], weights, drain;
     int tile_id[STAGES];
+    int n_local;      // tiles this CTA claimed (set once claiming ends), -1 before
     uint32_t tmem_base;
     int abort;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
+
+__device__ __forceinline__ bool aborted(Bars *sb) {
+    return *reinterpret_cast<volatile int *>(&sb->abort) != 0;
+}
+__device__ __forceinline__ void set_abort(Bars *sb, WsHeader *hdr) {
+    *reinterpret_cast<volatile int *>(&sb->abort) = 1;
+    latch_status(hdr, S5_ERR_TIMEOUT);
+}
 
 // Pipeline wait: bounded; gives up at once if another role already aborted.
 __device__ __forceinline__ bool pipe_wait(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        if (*reinterpret_cast<volatile int *>(&sb->abort)) return false;
+        if (aborted(sb)) return false;
         if (mbar_try_wait(bar, parity)) return true;
         if (global_ns() - t0 > PIPE_WAIT_NS) {
-            *reinterpret_cast<volatile int *>(&sb->abort) = 1;
-            latch_status(hdr, S5_ERR_TIMEOUT);
+            set_abort(sb, hdr);
             return false;
         }
     }
@@ -89,9 +104,27 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
+// Tile id of local tile i (-1 when this CTA has no i-th tile, -2 on abort).
+__device__ __forceinline__ int wait_tile(int i, Bars *sb, WsHeader *hdr) {
+    const int s = i % STAGES;
+    const uint32_t par = (i / STAGES) & 1;
+    if (mbar_try_wait(&sb->full_u[s], par)) return sb->tile_id[s];
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (aborted(sb)) return -2;
+        const int n = *reinterpret_cast<volatile int *>(&sb->n_local);
+        if (n >= 0 && i >= n) return -1;
+        if (mbar_try_wait(&sb->full_u[s], par)) return sb->tile_id[s];
+        if (global_ns() - t0 > PIPE_WAIT_NS) {
+            set_abort(sb, hdr);
+            return -2;
+        }
+    }
+}
+
 // Byte offset of bf16 element (row, col) in a K-major 128-byte-swizzle region
 // whose k-blocks (64 columns each) hold `rows` rows.
-__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col, uint32_t rows) {
+__host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t col, uint32_t rows) {
     const uint32_t kb = col >> 6, c = col & 63u;
     return kb * rows * 128u + row * 128u + (((c >> 3) ^ (row & 7u)) << 4) + ((c & 7u) << 1);
 }
@@ -174,6 +207,38 @@ __device__ float2 look_back(const float4 *rec, int B, int b, int c, int m, float
     }
 }
 
+// Loads the Re and Im columns [col, col+16) of this thread's lane.
+__device__ __forceinline__ void ld_chunk(uint32_t base, int col, uint32_t (&re)[16],
+                                         uint32_t (&im)[16]) {
+    tmem_ld16(base + col, re);
+    tmem_ld16(base + 64 + col, im);
+}
+
+// ---------------------------------------------------------------------------
+// Prep: bf16 operand images in the exact byte layout the MMA descriptors read.
+// ---------------------------------------------------------------------------
+__global__ void weight_images_kernel(const float2 *__restrict__ b_bar, const float2 *__restrict__ c_tilde,
+                                     unsigned char *__restrict__ img) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx < P_M * H_F / 2) {
+        // Bs: rows 0..P-1 = Re B_bar, rows P..2P-1 = Im B_bar, K = H
+        const int m = idx / (H_F / 2), h = 2 * (idx % (H_F / 2));
+        const float4 v = *reinterpret_cast<const float4 *>(b_bar + (size_t)m * H_F + h);
+        *reinterpret_cast<uint32_t *>(img + SM_BS + sw128(m, h, 2 * P_M)) = pack_bf16(v.x, v.z);
+        *reinterpret_cast<uint32_t *>(img + SM_BS + sw128(P_M + m, h, 2 * P_M)) = pack_bf16(v.y, v.w);
+    } else if (idx < P_M * H_F / 2 + H_F * P_M) {
+        // C': row h, columns (2m, 2m+1) = (2 Re C~[h][m], -2 Im C~[h][m]), K = 2P
+        const int k = idx - P_M * H_F / 2;
+        const int h = k / P_M, m = k % P_M;
+        const float2 cv = c_tilde[(size_t)h * P_M + m];
+        *reinterpret_cast<uint32_t *>(img + SM_CP + sw128(h, 2 * m, H_F)) =
+            pack_bf16(2.f * cv.x, -2.f * cv.y);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel.
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant__ CUtensorMap tmap_y,
               const TcArgs args) {
@@ -200,8 +265,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
             mbar_init(&sb->mma2_done[r], 1);
         }
         mbar_init(&sb->xready, 4);
-        mbar_init(&sb->xfree, 1);
+        mbar_init(&sb->xfree[0], 1);
+        mbar_init(&sb->xfree[1], 1);
+        mbar_init(&sb->weights, 1);
         mbar_init(&sb->drain, 1);
+        sb->n_local = -1;
         sb->abort = 0;
         fence_mbar_init();
         s_epoch = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
@@ -209,29 +277,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
         const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
         s_limit = 1000ull * (lim ? lim : 1000000u);
     }
-    if (warp == W_PROD && lane == 0) {
-        prefetch_tmap(&tmap_u);
-        prefetch_tmap(&tmap_y);
-    }
     if (warp == W_TMEM) {
         tmem_alloc(&sb->tmem_base, 512);
         tmem_relinquish();
     }
-    // Weights -> shared memory as bf16 K-major swizzled operands.
-    for (int idx = threadIdx.x; idx < P_M * H_F / 2; idx += THREADS) {
-        const int m = idx / (H_F / 2), h = 2 * (idx % (H_F / 2));
-        const float4 v = *reinterpret_cast<const float4 *>(args.b_bar + (size_t)m * H_F + h);
-        *reinterpret_cast<uint32_t *>(smem + SM_BS + sw128(m, h, 2 * P_M)) = pack_bf16(v.x, v.z);
-        *reinterpret_cast<uint32_t *>(smem + SM_BS + sw128(P_M + m, h, 2 * P_M)) =
-            pack_bf16(v.y, v.w);
-    }
-    for (int idx = threadIdx.x; idx < H_F * P_M; idx += THREADS) {
-        const int h = idx / P_M, m = idx % P_M;
-        const float2 cv = args.c_tilde[(size_t)h * P_M + m];
-        *reinterpret_cast<uint32_t *>(smem + SM_CP + sw128(h, 2 * m, H_F)) =
-            pack_bf16(2.f * cv.x, -2.f * cv.y);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -241,20 +290,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
     if (warp == W_PROD) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            prefetch_tmap(&tmap_u);
+            prefetch_tmap(&tmap_y);
+            mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
+            bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
+            bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
             int last_issue[STAGES] = {-1, -1, -1};
-            bool aborted = false;
-            for (int i = 0;; ++i) {
+            int i = 0;
+            for (;; ++i) {
                 const int s = i % STAGES;
-                if (i >= STAGES && !pipe_wait(&sb->empty_u[s], ((i / STAGES) - 1) & 1, sb, hdr)) {
-                    aborted = true;
-                    break;
-                }
+                if (i >= STAGES && !pipe_wait(&sb->empty_u[s], ((i / STAGES) - 1) & 1, sb, hdr)) break;
                 const int tile = (int)atomicAdd(&hdr->tile_counter, 1u);
-                if (tile >= args.ntiles) {
-                    sb->tile_id[s] = -1;
-                    mbar_arrive(&sb->full_u[s]);
-                    break;
-                }
+                if (tile >= args.ntiles) break;
                 sb->tile_id[s] = tile;
                 const int b = tile % B, c = tile / B;
                 unsigned char *dst = smem + SM_U + s * U_STAGE;
@@ -263,9 +310,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
                 tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
                 last_issue[s] = i;
             }
-            if (aborted)   // loads still in flight must land before the CTA exits
-                for (int s = 0; s < STAGES; ++s)
-                    if (last_issue[s] >= 0) drain_wait(&sb->full_u[s], (last_issue[s] / STAGES) & 1);
+            // consumers waiting for local tile i (never loaded) see the end here
+            *reinterpret_cast<volatile int *>(&sb->n_local) = i;
+            // copies still in flight must land before the CTA exits
+            drain_wait(&sb->weights, 0);
+            for (int s = 0; s < STAGES; ++s)
+                if (last_issue[s] >= 0) drain_wait(&sb->full_u[s], (last_issue[s] / STAGES) & 1);
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------------------ MMA issuer
@@ -273,79 +323,103 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
             const uint32_t idesc = idesc_bf16_f32(128, T_TOK);
             const uint32_t bs = smem_addr(smem + SM_BS), cp = smem_addr(smem + SM_CP);
             const uint32_t xs = smem_addr(smem + SM_X);
-            auto gemm2 = [&](int j) -> bool {
-                if (!pipe_wait(&sb->xready, j & 1, sb, hdr)) return false;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(j % REGIONS) * 128u;
-                for (int k = 0; k < 2 * P_M / 16; ++k)
-                    mma_bf16(d, sw128_kmajor_desc(cp + (k >> 2) * (H_F * 128) + (k & 3) * 32),
-                             sw128_kmajor_desc(xs + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
-                             idesc, k > 0);
-                mma_commit(&sb->mma2_done[j % REGIONS]);
-                mma_commit(&sb->xfree);
-                return true;
-            };
-            bool ok = true;
-            int i = 0;
-            for (;; ++i) {
-                const int s = i % STAGES, r = i % REGIONS;
-                if (!pipe_wait(&sb->full_u[s], (i / STAGES) & 1, sb, hdr)) { ok = false; break; }
-                if (sb->tile_id[s] < 0) break;
-                if (i >= REGIONS && !pipe_wait(&sb->tmem_empty[r], ((i / REGIONS) - 1) & 1, sb, hdr)) {
-                    ok = false;
+            bool ok = pipe_wait(&sb->weights, 0, sb, hdr);
+            int g1 = 0, g2 = 0;          // next tile for GEMM1 / GEMM2
+            int n_end = -1;              // tiles of this CTA, once known
+            unsigned long long t0 = global_ns();
+            while (ok) {
+                bool progress = false;
+                // GEMM1 of tile g1: u tile landed and its TMEM region is free
+                if (n_end < 0 || g1 < n_end) {
+                    const int s = g1 % STAGES, r = g1 % REGIONS;
+                    const int n = *reinterpret_cast<volatile int *>(&sb->n_local);
+                    if (n >= 0 && g1 >= n) {
+                        n_end = n;
+                    } else if (mbar_test_wait(&sb->full_u[s], (g1 / STAGES) & 1) &&
+                               (g1 < REGIONS ||
+                                mbar_test_wait(&sb->tmem_empty[r], ((g1 / REGIONS) - 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t ub = smem_addr(smem + SM_U + s * U_STAGE);
+                        for (int mb = 0; mb < 2; ++mb)
+                            for (int k = 0; k < H_F / 16; ++k)
+                                mma_bf16(tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u,
+                                         sw128_kmajor_desc(bs + (k >> 2) * (2 * P_M * 128) +
+                                                           mb * (P_M * 128) + (k & 3) * 32),
+                                         sw128_kmajor_desc(ub + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
+                                         idesc, k > 0);
+                        mma_commit(&sb->tmem_full[r]);
+                        ++g1;
+                        progress = true;
+                    }
+                }
+                // GEMM2 of tile g2: its scan wrote X
+                if (g2 < g1 && mbar_test_wait(&sb->xready, g2 & 1)) {
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(g2 % REGIONS) * 128u;
+                    for (int k = 0; k < 2 * P_M / 16; ++k)
+                        mma_bf16(d, sw128_kmajor_desc(cp + (k >> 2) * (H_F * 128) + (k & 3) * 32),
+                                 sw128_kmajor_desc(xs + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
+                                 idesc, k > 0);
+                    mma_commit(&sb->mma2_done[g2 % REGIONS]);
+                    mma_commit(&sb->xfree[g2 & 1]);
+                    ++g2;
+                    progress = true;
+                }
+                if (n_end >= 0 && g2 >= n_end) break;
+                if (progress) {
+                    t0 = global_ns();
+                } else if (aborted(sb)) {
+                    break;
+                } else if (global_ns() - t0 > PIPE_WAIT_NS) {
+                    set_abort(sb, hdr);
                     break;
                 }
-                tc_fence_after();
-                const uint32_t ub = smem_addr(smem + SM_U + s * U_STAGE);
-                for (int mb = 0; mb < 2; ++mb)
-                    for (int k = 0; k < H_F / 16; ++k)
-                        mma_bf16(tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u,
-                                 sw128_kmajor_desc(bs + (k >> 2) * (2 * P_M * 128) + mb * (P_M * 128) +
-                                                   (k & 3) * 32),
-                                 sw128_kmajor_desc(ub + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
-                                 idesc, k > 0);
-                mma_commit(&sb->tmem_full[r]);
-                if (i >= 1 && !gemm2(i - 1)) { ok = false; break; }
             }
-            if (ok && i >= 1) gemm2(i - 1);
             // every MMA issued must complete before TMEM is freed
             mma_commit(&sb->drain);
             drain_wait(&sb->drain, 0);
         }
-    } else if (warp >= W_SCAN && warp < W_SCAN + 4) {
-        // ------------------------------------------------------------ scan
-        const int qd = warp - W_SCAN;
+    } else if (warp >= W_SCAN && warp < W_SCAN + 8) {
+        // ------------------------------------------------------------ scan groups
+        const int grp = (warp - W_SCAN) >> 2;   // 0: even local tiles, 1: odd
+        const int qd = (warp - W_SCAN) & 3;     // TMEM lane quarter
         const int m = 32 * qd + lane;
         const float2 lb = args.lambda_bar[m];
         float2 lbT = lb;
         for (int e = 1; e < T_TOK; e <<= 1) lbT = cmul(lbT, lbT);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         unsigned char *xw = smem + SM_X + qd * (T_TOK * 128);
-        const uint32_t xcol = ((uint32_t)lane * 4u);   // byte of (Re, Im) in this warp's k-block row
-        for (int i = 0;; ++i) {
-            const int s = i % STAGES, r = i % REGIONS;
-            if (!pipe_wait(&sb->full_u[s], (i / STAGES) & 1, sb, hdr)) break;
-            const int tile = sb->tile_id[s];
+        const uint32_t xcol = (uint32_t)lane * 4u;   // byte of (Re, Im) in this warp's k-block row
+        for (int i = grp;; i += 2) {
+            const int tile = wait_tile(i, sb, hdr);
             if (tile < 0) break;
             const int b = tile % B, c = tile / B;
             const int Tc = min(T_TOK, L - c * T_TOK);
+            const int r = i % REGIONS;
             if (!pipe_wait(&sb->tmem_full[r], (i / REGIONS) & 1, sb, hdr)) break;
             tc_fence_after();
             const uint32_t col0 = lane_base + (uint32_t)r * 128u;
 
             // pass 1: end state of the tile from a zero start
             float2 E = make_float2(0.f, 0.f);
-#pragma unroll 1
-            for (int ch = 0; ch < T_TOK / 16; ++ch) {
-                if (ch * 16 >= Tc) break;
+            {
                 uint32_t re[16], im[16];
-                tmem_ld16(col0 + ch * 16, re);
-                tmem_ld16(col0 + 64 + ch * 16, im);
+                ld_chunk(col0, 0, re, im);
                 tmem_wait_ld();
-                const int n = Tc - ch * 16;
+#pragma unroll 1
+                for (int ch = 0; ch < T_TOK / 16; ++ch) {
+                    if (ch * 16 >= Tc) break;
+                    float2 v[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (k < n) E = cfma(lb, E, make_float2(__uint_as_float(re[k]), __uint_as_float(im[k])));
+                    for (int k = 0; k < 16; ++k)
+                        v[k] = make_float2(__uint_as_float(re[k]), __uint_as_float(im[k]));
+                    if ((ch + 1) * 16 < Tc) ld_chunk(col0, (ch + 1) * 16, re, im);
+                    const int n = Tc - ch * 16;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (k < n) E = cfma(lb, E, v[k]);
+                    tmem_wait_ld();
+                }
             }
             const float2 A = (Tc == T_TOK) ? lbT : cpow(lb, Tc);
             const bool publish = s_drop != (unsigned)(tile + 1);
@@ -361,27 +435,32 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
             if (publish) st_v4(my, inc.x, inc.y, 0.f, __uint_as_float((epoch << 2) | FLAG_INCL));
 
             // pass 2: states from the carry, written as the bf16 GEMM2 operand
-            if (i >= 1 && !pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr)) break;
+            if (i >= 1 && !pipe_wait(&sb->xfree[(i - 1) & 1], ((i - 1) >> 1) & 1, sb, hdr)) break;
             float2 x = carry;
-#pragma unroll 1
-            for (int ch = 0; ch < T_TOK / 16; ++ch) {
+            {
                 uint32_t re[16], im[16];
-                const bool live = ch * 16 < Tc;
-                if (live) {
-                    tmem_ld16(col0 + ch * 16, re);
-                    tmem_ld16(col0 + 64 + ch * 16, im);
-                    tmem_wait_ld();
-                }
+                ld_chunk(col0, 0, re, im);
+                tmem_wait_ld();
+#pragma unroll 1
+                for (int ch = 0; ch < T_TOK / 16; ++ch) {
+                    const bool live = ch * 16 < Tc;
+                    float2 v[16];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int t = ch * 16 + k;
-                    uint32_t v = 0;
-                    if (live && t < Tc) {
-                        x = cfma(lb, x, make_float2(__uint_as_float(re[k]), __uint_as_float(im[k])));
-                        v = pack_bf16(x.x, x.y);
+                    for (int k = 0; k < 16; ++k)
+                        v[k] = make_float2(__uint_as_float(re[k]), __uint_as_float(im[k]));
+                    if ((ch + 1) * 16 < Tc) ld_chunk(col0, (ch + 1) * 16, re, im);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const int t = ch * 16 + k;
+                        uint32_t pv = 0;
+                        if (live && t < Tc) {
+                            x = cfma(lb, x, v[k]);
+                            pv = pack_bf16(x.x, x.y);
+                        }
+                        *reinterpret_cast<uint32_t *>(xw + t * 128 + (((xcol >> 4) ^ (uint32_t)(t & 7)) << 4) +
+                                                      (xcol & 15u)) = pv;
                     }
-                    *reinterpret_cast<uint32_t *>(xw + t * 128 + ((((xcol >> 4) ^ (uint32_t)(t & 7))) << 4) +
-                                                  (xcol & 15u)) = v;
+                    tmem_wait_ld();
                 }
             }
             if (c == args.nchunks - 1 && args.x_last) args.x_last[(size_t)b * P_M + m] = x;
@@ -399,10 +478,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
         const uint32_t hkb = (uint32_t)h >> 6, hc = (uint32_t)h & 63u;
         const bool leader = (threadIdx.x == W_EPI * 32);
         for (int i = 0;; ++i) {
-            const int s = i % STAGES, r = i % REGIONS;
-            if (!pipe_wait(&sb->full_u[s], (i / STAGES) & 1, sb, hdr)) break;
-            const int tile = sb->tile_id[s];
+            const int tile = wait_tile(i, sb, hdr);
             if (tile < 0) break;
+            const int s = i % STAGES, r = i % REGIONS;
             if (!pipe_wait(&sb->mma2_done[r], (i / REGIONS) & 1, sb, hdr)) break;
             tc_fence_after();
             uint32_t yv[T_TOK];
@@ -416,13 +494,24 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant_
             if (lane == 0) mbar_arrive(&sb->tmem_empty[r]);
             unsigned char *stage = smem + SM_U + s * U_STAGE + hkb * (T_TOK * 128);
 #pragma unroll
-            for (int t = 0; t < T_TOK; ++t) {
-                __nv_bfloat16 *p = reinterpret_cast<__nv_bfloat16 *>(
-                    stage + t * 128 + (((hc >> 3) ^ (uint32_t)(t & 7)) << 4) + ((hc & 7u) << 1));
-                *p = __float2bfloat16_rn(fmaf(dh, __bfloat162float(*p), __uint_as_float(yv[t])));
+            for (int t0 = 0; t0 < T_TOK; t0 += 16) {
+                __nv_bfloat16 uvals[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int t = t0 + k;
+                    uvals[k] = *reinterpret_cast<const __nv_bfloat16 *>(
+                        stage + t * 128 + (((hc >> 3) ^ (uint32_t)(t & 7)) << 4) + ((hc & 7u) << 1));
+                }
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int t = t0 + k;
+                    *reinterpret_cast<__nv_bfloat16 *>(
+                        stage + t * 128 + (((hc >> 3) ^ (uint32_t)(t & 7)) << 4) + ((hc & 7u) << 1)) =
+                        __float2bfloat16_rn(fmaf(dh, __bfloat162float(uvals[k]), __uint_as_float(yv[t])));
+                }
             }
             fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_sync(1, 128);
             if (leader) {
                 const int b = tile % B, c = tile / B;
                 unsigned char *src = smem + SM_U + s * U_STAGE;
@@ -491,8 +580,12 @@ cudaError_t launch_forward_tc(const TcArgs &a, const void *u, void *y, cudaStrea
                               int num_sms) {
     CUtensorMap mu, my;
     if (!make_map(&mu, u, a.B, a.L) || !make_map(&my, y, a.B, a.L)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_REQUEST);
+    const int words = P_M * H_F / 2 + H_F * P_M;
+    weight_images_kernel<<<(words + 255) / 256, 256, 0, st>>>(a.b_bar, a.c_tilde, a.ws.wimg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_REQUEST);
     if (e != cudaSuccess) return e;
     int grid = num_sms < a.ntiles ? num_sms : a.ntiles;
     fwd_tc_kernel<<<grid, THREADS, SMEM_REQUEST, st>>>(mu, my, a);

@@ -16,7 +16,8 @@ namespace s5 {
 // zero start) and then its inclusive end state.  Layout (each region 256-byte
 // aligned):
 //   header (256 B) | flags [ntiles] u32 | agg [ntiles][P] float4 |
-//   incl [ntiles][P] float2 | mode constants [P] ModeConst
+//   incl [ntiles][P] float2 | mode constants [P] ModeConst |
+//   operand images [8*P*H bytes] (bf16 weights of the tensor-core path)
 // Flags carry a launch epoch in their upper 30 bits so that a workspace needs
 // no clearing between calls: the last CTA of every launch bumps the epoch and
 // resets the tile counters.
@@ -54,14 +55,20 @@ struct WsLayout {
     float4 *agg;
     float2 *incl;
     ModeConst *modes;
+    unsigned char *wimg;
 };
 
-__host__ __device__ inline size_t ws_bytes(long long ntiles, int P) {
+// Bytes of the bf16 operand images: B_bar split into 2P rows of H, and C' as
+// H rows of 2P, 2 bytes each.
+__host__ __device__ inline size_t wimg_bytes(int P, int H) { return (size_t)8 * P * H; }
+
+__host__ __device__ inline size_t ws_bytes(long long ntiles, int P, int H) {
     size_t s = 256;
     s += align256(sizeof(unsigned int) * (size_t)ntiles);
     s += align256(sizeof(float4) * (size_t)ntiles * P);
     s += align256(sizeof(float2) * (size_t)ntiles * P);
     s += align256(sizeof(ModeConst) * (size_t)P);
+    s += 1024 + wimg_bytes(P, H);   // images start 1024-byte aligned
     return s;
 }
 
@@ -77,6 +84,10 @@ inline WsLayout ws_layout(void *base, long long ntiles, int P) {
     w.incl = reinterpret_cast<float2 *>(p);
     p += align256(sizeof(float2) * (size_t)ntiles * P);
     w.modes = reinterpret_cast<ModeConst *>(p);
+    p += align256(sizeof(ModeConst) * (size_t)P);
+    // 1024-byte alignment keeps the swizzle pattern of the images intact
+    p = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+    w.wimg = reinterpret_cast<unsigned char *>(p);
     return w;
 }
 
