@@ -131,6 +131,7 @@ s5_status run_tc(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_
     a.b_bar = b_bar;
     a.c_tilde = c_tilde;
     a.d = d;
+    a.y = y;
     a.x0 = reinterpret_cast<const float2 *>(x0);
     a.x_last = reinterpret_cast<float2 *>(x_last);
     a.B = B;
@@ -139,7 +140,7 @@ s5_status run_tc(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_
     a.ntiles = (int)ntiles;
     a.ws = s5::ws_layout(workspace, ntiles, P);
     (void)H;
-    cudaError_t e = s5::launch_forward_tc(a, u, y, st, sms);
+    cudaError_t e = s5::launch_forward_tc(a, u, st, sms);
     return e == cudaSuccess ? S5_OK : cuda_fail(e);
 }
 

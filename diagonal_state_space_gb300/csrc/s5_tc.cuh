@@ -11,6 +11,7 @@ struct TcArgs {
     const float2 *b_bar;       // [P][H]
     const float2 *c_tilde;     // [H][P]
     const float *d;            // [H]
+    void *y;                   // [B][L][H] bf16
     const float2 *x0;          // [B][P] or null
     float2 *x_last;            // [B][P] or null
     int B, L, nchunks, ntiles;
@@ -19,7 +20,6 @@ struct TcArgs {
 
 // The tensor-core kernel covers H = 128, P = 128 with bf16 u, y and projections.
 bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16);
-cudaError_t launch_forward_tc(const TcArgs &a, const void *u, void *y, cudaStream_t st,
-                              int num_sms);
+cudaError_t launch_forward_tc(const TcArgs &a, const void *u, cudaStream_t st, int num_sms);
 
 }  // namespace s5
