@@ -4,30 +4,38 @@
 // 1, 3, 4; summary "SIMPLIFIED STATE SPACE LAYERS ...", App. A and App. H):
 //   Bu_k = B_bar u_k,  x_k = lambda_bar * x_{k-1} + Bu_k,  y_k = 2 Re(C~ x_k) + D u_k.
 //
-// A prep kernel writes the bf16 operand images of B_bar and C' into the
-// workspace.  Then one persistent CTA per SM (a cooperative launch, so every
-// CTA is resident) takes the tiles k, k+G, k+2G, ... of 64 tokens (G = grid):
-// all CTAs work through the same "wave" of G tiles at the same time, so a
-// tile's predecessors in its sequence are same-wave tiles being scanned
-// concurrently, and the look-back waits on no other CTA's queue.  Each CTA
-// runs a warp-specialised pipeline over its tiles:
-//   warp 0        TMA: u tile [64 tokens x 128 features] bf16 -> smem (4 stages);
-//                 bulk copy of the two weight images at start-up
-//   warp 1        tcgen05.mma issuer, driven by whichever input is ready:
-//                   GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T      (into TMEM)
-//                   GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T      (into TMEM)
-//   warp 2        TMEM allocation (512 columns: 4 regions of 128)
-//   warps 4-7     scan: thread = mode = TMEM lane, one tile ahead:
-//                 pass 1 of tile i+1 folds its 64 steps from zero and
-//                 publishes the aggregate; the look-back loads for tile i+1
-//                 are issued; pass 2 of tile i reruns from its carry (two
-//                 interleaved 32-step chains) and writes x_k as bf16 into the
-//                 GEMM2 operand X [64 x 2P]; then the look-back of tile i+1
-//                 resolves and its inclusive state is published.
-//   warps 8-11    epilogue: thread = feature = TMEM lane of GEMM2;
-//                 y = D2 + D*u with u read from the stage (the stage is free
-//                 once GEMM1 and the epilogue have read it), stored as bf16
-//                 with one 64-byte segment per warp and token.
+// Work split.  A sequence of nchunks tiles (64 tokens each) is spread over W
+// "lanes" (CTAs): lane p of sequence b takes chunks p, p+W, p+2W, ...  With
+// Lam = lambda_bar^64 and E(q) the end state of chunk q from a zero start, the
+// state entering chunk c of a lane follows from its own previous chunk c-W:
+//   S(c) = Lam^(W-1) x_end(c-W) + sum_{q=c-W+1}^{c-1} Lam^(c-1-q) E(q),
+// and for the lane's first chunk (c < W): S(c) = Lam^c x0 + sum_{q<c} Lam^(c-1-q) E(q).
+// Every E(q) is known once chunk q's own scan (pass 1) has run, so no tile
+// waits for another tile's final state: there is no carry chain across CTAs,
+// only W-1 aggregate records to read per tile.  Grid: B*W CTAs (one per SM,
+// cooperative launch so that all are resident); when B exceeds the SM count,
+// W = 1 and each CTA takes whole sequences.
+//
+// Each CTA runs a warp-specialised pipeline over its tiles:
+//   warps 0-3   TMA and tcgen05.mma issue (one thread each):
+//                 TMA: u tile [64 tokens x 128 features] bf16 -> smem (4
+//                 stages, freed as soon as GEMM1 has read it); bulk copy of
+//                 the two weight images at start-up
+//                 GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T      (into TMEM)
+//                 GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T      (into TMEM)
+//               Each GEMM is split over two threads (rows / k-steps), so that
+//               four chains of dependent MMAs are in flight.  Warp 2 also
+//               allocates TMEM (512 columns: 4 regions of 128).
+//   warps 4-7   scan, thread = mode = TMEM lane, pass 1 two tiles ahead: pass 1
+//               of tile i+2 (end state from zero, published as the tile's
+//               aggregate record), then pass 2 of tile i from its carry (two
+//               interleaved 32-step chains), written as bf16 into the GEMM2
+//               operand X [64 x 2P]
+//   warps 8-11  epilogue, thread = feature = TMEM lane of GEMM2:
+//               y = D2 + D*u (u re-read through L2), bf16 stores
+//   warps 12-15 carry windows, thread = mode: fold the aggregate records that
+//               each tile's carry needs into a shared-memory slot (two slots),
+//               running ahead of the scan.
 // Bs holds B_bar split into real rows (0..P-1) and imaginary rows (P..2P-1);
 // C' interleaves (2 Re C~, -2 Im C~) so that K = 2P of GEMM2 pairs with X's
 // interleaved (Re x, Im x): sum_k C'[h][k] X[t][k] = 2 Re(C~ x_t)[h].
@@ -52,8 +60,11 @@ constexpr int H_F = 128;                // features
 constexpr int P_M = 128;                // stored complex modes
 constexpr int STAGES = 4;
 constexpr int REGIONS = 4;              // TMEM regions of 128 columns
-constexpr int THREADS = 384;
-constexpr int W_PROD = 0, W_MMA = 1, W_TMEM = 2, W_SCAN = 4, W_EPI = 8;
+constexpr int THREADS = 512;
+constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;
+constexpr int W_MAX = 64;               // lanes per sequence at most
+constexpr int RB = 18;                  // aggregate records loaded per round
+constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps
 
 constexpr uint32_t BS_BYTES = 2 * 2 * P_M * 128;       // [2 kb][2P rows][128 B]
 constexpr uint32_t CP_BYTES = 4 * H_F * 128;           // [4 kb][H rows][128 B]
@@ -62,10 +73,13 @@ constexpr uint32_t SM_CP = SM_BS + BS_BYTES;
 constexpr uint32_t SM_U = SM_CP + CP_BYTES;            // [stage][2 kb][64 rows][128 B]
 constexpr uint32_t U_STAGE = 2 * T_TOK * 128;
 constexpr uint32_t SM_X = SM_U + STAGES * U_STAGE;     // [4 kb][64 rows][128 B]
-constexpr uint32_t SM_BAR = SM_X + 4 * T_TOK * 128;
-constexpr uint32_t SM_TOTAL = SM_BAR + 512;
-constexpr uint32_t SMEM_REQUEST = SM_TOTAL + 1024;     // slack for 1024-B alignment
-static_assert(SMEM_REQUEST <= 227 * 1024, "shared memory budget");
+constexpr uint32_t SM_CARRY = SM_X + 4 * T_TOK * 128;  // [2 slots][P] float2
+constexpr uint32_t SM_BAR = SM_CARRY + 2 * P_M * 8;
+constexpr uint32_t SM_TOTAL = SM_BAR + 256;
+// Dynamic shared memory is requested up to the per-block limit; the slack
+// absorbs the rounding of its base up to 1024 bytes (checked at run time).
+constexpr uint32_t SMEM_REQUEST = 227 * 1024;
+static_assert(SM_TOTAL <= SMEM_REQUEST, "shared memory budget");
 static_assert(BS_BYTES + CP_BYTES == 8 * P_M * H_F, "image size");
 
 constexpr unsigned long long PIPE_WAIT_NS = 2000000000ull;   // 2 s per pipeline wait
@@ -75,11 +89,13 @@ struct Bars {
     uint64_t full_u[STAGES], empty_u[STAGES];
     uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], mma2_done[REGIONS];
     uint64_t xready, xfree, weights, drain;
-    int n_local;      // tiles of this CTA
+    uint64_t carry_full[2], carry_empty[2];
+    unsigned long long limit_ns;   // aggregate-record wait limit
     uint32_t tmem_base;
+    unsigned epoch, drop;
     int abort;
 };
-static_assert(sizeof(Bars) <= 512, "barrier block");
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 __device__ __forceinline__ bool aborted(Bars *sb) {
     return *reinterpret_cast<volatile int *>(&sb->abort) != 0;
@@ -114,12 +130,19 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-// Tile id of local tile i once its u tile has landed (-1 when this CTA has
-// no i-th tile, -2 on abort).
-__device__ __forceinline__ int wait_tile(int i, Bars *sb, WsHeader *hdr) {
-    if (i >= sb->n_local) return -1;
-    if (!pipe_wait(&sb->full_u[i % STAGES], (i / STAGES) & 1, sb, hdr)) return -2;
-    return (int)blockIdx.x + i * (int)gridDim.x;
+// Barrier of `threads` threads that also returns the AND of `v` over them, so
+// that the warps taking part leave a loop together.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
 }
 
 // Byte offset of bf16 element (row, col) in a K-major 128-byte-swizzle region
@@ -134,30 +157,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Carry records are read and written with GPU-scope relaxed 16-byte accesses
-// (a record is written whole, so a reader sees its state and value together;
-// system-scope accesses would be needlessly slow on a host-coherent GPU).
-__device__ __forceinline__ float4 ld_record(const float4 *p) {
-    float4 v;
-    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_record(float4 *p, float a, float b, float c, float d) {
-    asm volatile("st.relaxed.gpu.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-}
-
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ float2 cpow(float2 a, int n) {
@@ -170,96 +171,112 @@ __device__ __forceinline__ float2 cpow(float2 a, int n) {
     return r;
 }
 
-// Carry into tile (b, c) from the per-mode records of tiles (b, c-1), (b, c-2)...
-// Each record is one 16-byte word {value.re, value.im, 0, epoch<<2 | state}:
-// state 1 = aggregate (end state from zero; the tile's multiplier is
-// lambda_bar^64 since only a sequence's last tile can be short), 2 = inclusive
-// end state.  LB_WIN predecessors are read per round.
-constexpr int LB_WIN = 8;    // records loaded an iteration ahead
-constexpr int LB_WIN2 = 12;  // records loaded when the look-back resolves (together: 20,
-                             // a whole wave of one sequence, G / B = 19 chunks, in one round)
-// Loads the records of chunks j, j-1, ..., j-LB_WIN+1 of this mode.
-__device__ __forceinline__ void lb_issue(float4 (&v)[LB_WIN], const float4 *col, size_t stride, int j) {
-    const float4 *pj = col + (size_t)j * stride;
-#pragma unroll
-    for (int w = 0; w < LB_WIN; ++w)
-        v[w] = (j - w >= 0) ? ld_record(pj - (size_t)w * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+// ---------------------------------------------------------------------------
+// Aggregate records.  Tile (b, c) (index b * nchunks + c) publishes, per mode,
+// one 16-byte word {E.re, E.im, 0, epoch << 2 | FLAG_AGG}, written and read
+// whole with GPU-scope relaxed vector accesses: a reader that sees this
+// launch's tag sees the value stored with it, so one load both checks and
+// fetches a record (no separate flag, no fence, one memory round trip).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_record(const float4 *p) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_record(float4 *p, float2 e, unsigned tag) {
+    asm volatile("st.relaxed.gpu.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(e.x), "f"(e.y),
+                 "f"(0.f), "f"(__uint_as_float(tag))
+                 : "memory");
 }
 
-// Folds one window of records into (acc, mult), newest first.  Returns 1 when
-// an inclusive record ended the chain, 0 when the window was used up, -1 when
-// a record was not ready (j then names the first record still needed).
-template <int W>
-__device__ __forceinline__ int lb_fold(const float4 (&v)[W], int &j, float2 &acc, float2 &mult,
-                                       float2 lbT, unsigned agg, unsigned incl) {
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-        if (j < 0) return 0;
-        const unsigned st = __float_as_uint(v[w].w);
-        const bool is_incl = st == incl;
-        if (!(is_incl || st == agg)) return -1;
-        acc = cfma(mult, make_float2(v[w].x, v[w].y), acc);
-        if (is_incl) return 1;
-        mult = cmul(mult, lbT);
-        --j;
+// Lane geometry: CTA k of G.  W > 1: one lane (b = k % B, p = k / B) with
+// chunks p, p + W, ...  W == 1: sequences k, k + G, ..., every chunk.
+struct Lane {
+    int B, W, G, k, nchunks;
+    __device__ __forceinline__ int count() const {
+        if (W > 1) return (nchunks - k / B + W - 1) / W;
+        return (k < B ? (B - k + G - 1) / G : 0) * nchunks;
     }
-    return 0;
-}
-
-// Carry of chunk j+1: folds the records of chunks j, j-1, ... until an
-// inclusive one.  v holds the LB_WIN records from chunk j down, loaded
-// earlier by lb_issue; the next LB_WIN2 are loaded on entry so that their
-// latency overlaps the first fold, and further windows are loaded as needed.
-__device__ float2 lb_finish(float4 (&v)[LB_WIN], const float4 *col, size_t stride, int j,
-                            float2 lbT, unsigned epoch, WsHeader *hdr, unsigned long long limit,
-                            int tile) {
-    float2 acc = make_float2(0.f, 0.f), mult = make_float2(1.f, 0.f);
-    const unsigned agg = (epoch << 2) | FLAG_AGG, incl = (epoch << 2) | FLAG_INCL;
-    float4 v2[LB_WIN2];
-    {
-        const float4 *pj = col + (size_t)(j - LB_WIN) * stride;
-#pragma unroll
-        for (int w = 0; w < LB_WIN2; ++w)
-            v2[w] = (j - LB_WIN - w >= 0) ? ld_record(pj - (size_t)w * stride)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    int rc = lb_fold<LB_WIN>(v, j, acc, mult, lbT, agg, incl);
-    if (rc == 1) return acc;
-    if (rc == 0) {
-        rc = lb_fold<LB_WIN2>(v2, j, acc, mult, lbT, agg, incl);
-        if (rc == 1) return acc;
-    }
-    // slow path: chains longer than one wave, or records not yet published
-    unsigned long long t0 = 0;
-    bool timing = false;
-    int last_j = j;
-    for (;;) {
-        if (j < 0) return acc;
-        lb_issue(v, col, stride, j);
-        rc = lb_fold<LB_WIN>(v, j, acc, mult, lbT, agg, incl);
-        if (rc == 1) return acc;
-        if (j < last_j) {
-            timing = false;
-            last_j = j;
-            continue;
+    __device__ __forceinline__ void tile(int i, int &b, int &c) const {
+        if (W > 1) {
+            b = k % B;
+            c = k / B + i * W;
+        } else {
+            b = k + (i / nchunks) * G;
+            c = i % nchunks;
         }
+    }
+};
+
+// Folds the aggregate records that the carry of chunk c (sequence b) needs
+// for mode m: sum_q Lam^(c-1-q) E(q) over the window q in [c-W+1, c) (or
+// [0, c) when c < W), Horner from the oldest record.  The newest record of the
+// window (the last one to be published, as lanes advance together) is polled
+// alone, with backoff, before the window is read; records still missing then
+// are re-read.  A wait that runs out latches S5_ERR_TIMEOUT and folds zeros in
+// place of the missing records, so that the launch still completes.
+__device__ float2 fold_window(const float4 *rec, int b, int c, int nchunks, int W, int m, float2 Lam,
+                              unsigned tag, WsHeader *hdr, unsigned long long limit, bool &gave_up) {
+    const int lo = c < W ? 0 : c - W + 1;
+    const int n = c < W ? c : W - 1;
+    float2 acc = make_float2(0.f, 0.f);
+    if (n == 0) return acc;
+    const size_t seq = (size_t)b * nchunks;
+    unsigned long long t0 = 0;
+    unsigned backoff = 64;
+    bool timing = false;
+    // wait for the newest record
+    while (!gave_up && __float_as_uint(ld_record(rec + (seq + c - 1) * P_M + m).w) != tag) {
         if (!timing) {
             t0 = global_ns();
             timing = true;
         } else if (global_ns() - t0 > limit) {
             latch_status(hdr, S5_ERR_TIMEOUT);
-            atomicCAS(&hdr->timeout_tile, 0u, (unsigned)tile + 1);
-            return acc;
+            atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + c) + 1u);
+            gave_up = true;
+            break;
         }
-        __nanosleep(64);
+        __nanosleep(backoff);
+        if (backoff < 1024) backoff <<= 1;
     }
-}
-
-// Loads the Re and Im columns [col, col+16) of this thread's lane.
-__device__ __forceinline__ void ld_chunk(uint32_t base, int col, uint32_t (&re)[16],
-                                         uint32_t (&im)[16]) {
-    tmem_ld16(base + col, re);
-    tmem_ld16(base + 64 + col, im);
+    for (int base = 0; base < n; base += RB) {
+        const int nr = min(RB, n - base);
+        const float4 *rp = rec + (seq + lo + base) * P_M + m;
+        float4 v[RB];
+        for (;;) {
+            bool ready = true;
+#pragma unroll
+            for (int w = 0; w < RB; ++w) {
+                v[w] = (w < nr) ? ld_record(rp + (size_t)w * P_M) : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (w < nr && __float_as_uint(v[w].w) != tag) ready = false;
+            }
+            if (ready) break;
+            if (gave_up) {
+#pragma unroll
+                for (int w = 0; w < RB; ++w)
+                    if (__float_as_uint(v[w].w) != tag) v[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+                break;
+            }
+            if (!timing) {
+                t0 = global_ns();
+                timing = true;
+            } else if (global_ns() - t0 > limit) {
+                latch_status(hdr, S5_ERR_TIMEOUT);
+                atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + c) + 1u);
+                gave_up = true;
+                continue;   // one more pass zeroes what is missing
+            }
+            __nanosleep(backoff);
+            if (backoff < 1024) backoff <<= 1;
+        }
+#pragma unroll
+        for (int w = 0; w < RB; ++w)
+            if (w < nr) acc = cfma(Lam, acc, make_float2(v[w].x, v[w].y));
+    }
+    return acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -267,12 +284,8 @@ __device__ __forceinline__ void ld_chunk(uint32_t base, int col, uint32_t (&re)[
 // [col0, col0+64) hold Re(Bu_t), [col0+64, col0+128) hold Im(Bu_t).
 // ---------------------------------------------------------------------------
 struct ScanConsts {
-    float2 lb, lb8, lb16, lb32, lb64;   // lambda_bar and its powers
+    float2 lb, lb32, lb64;   // lambda_bar and its powers
 };
-
-__device__ __forceinline__ float2 tmem_pair(const uint32_t (&re)[16], const uint32_t (&im)[16], int k) {
-    return make_float2(__uint_as_float(re[k]), __uint_as_float(im[k]));
-}
 
 // Full tile: end state from zero over tokens 0..31 (elo) and 0..63 (returned),
 // as two interleaved 32-step chains over tokens 0..31 and 32..63.
@@ -302,12 +315,13 @@ __device__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
 #pragma unroll 1
     for (int ch = 0; ch * 16 < Tc; ++ch) {
         uint32_t re[16], im[16];
-        ld_chunk(col0, ch * 16, re, im);
+        tmem_ld16(col0 + ch * 16, re);
+        tmem_ld16(col0 + 64 + ch * 16, im);
         tmem_wait_ld();
         const int n = Tc - ch * 16;
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-            if (t < n) e = cfma(lb, e, tmem_pair(re, im, t));
+            if (t < n) e = cfma(lb, e, make_float2(__uint_as_float(re[t]), __uint_as_float(im[t])));
     }
     return e;
 }
@@ -346,14 +360,15 @@ __device__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb,
         uint32_t re[16], im[16];
         const bool live = ch * 16 < Tc;
         if (live) {
-            ld_chunk(col0, ch * 16, re, im);
+            tmem_ld16(col0 + ch * 16, re);
+            tmem_ld16(col0 + 64 + ch * 16, im);
             tmem_wait_ld();
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
             uint32_t pv = 0;
             if (live && ch * 16 + t < Tc) {
-                x = cfma(lb, x, tmem_pair(re, im, t));
+                x = cfma(lb, x, make_float2(__uint_as_float(re[t]), __uint_as_float(im[t])));
                 pv = pack_bf16(x.x, x.y);
             }
             sts32(xb[t & 7] + (uint32_t)((ch * 16 + t) >> 3) * 1024u, pv);
@@ -362,60 +377,28 @@ __device__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb,
     return x;
 }
 
-// One tile of the scan stage.
+// One tile in flight in the scan warps.
 struct ScanTile {
-    int tile, b, c, Tc, r;
-    float2 E, elo, carry;
-    bool pending;   // look-back still to resolve
+    int g, b, c, Tc, r;
+    float2 elo;
 };
 
-// Everything the scan warps need that does not change from tile to tile.
-struct ScanCtx {
-    ScanConsts kc;
-    uint32_t lane_base;
-    float4 *rec;
-    const float2 *x0;
-    size_t stride;
-    int B, L, m;
-    unsigned epoch, drop, agg_word, incl_word;
-    unsigned long long limit;
-    WsHeader *hdr;
-};
-
-// Pass 1 of a tile whose D1 has landed; publishes its aggregate (or, for a
-// sequence's first chunk, its inclusive state) and issues its look-back loads.
-__device__ __forceinline__ void scan_front(const ScanCtx &x, ScanTile &T) {
-    const uint32_t col0 = x.lane_base + (uint32_t)T.r * 128u;
+// Pass 1 of local tile i: waits for its GEMM1, runs pass 1 and publishes the
+// tile's aggregate record for this mode.  Returns false if the wait gave up.
+__device__ __forceinline__ bool scan_front(ScanTile &T, int i, const Lane &ln, int L, uint32_t lane_base,
+                                           const ScanConsts &kc, float4 *rec, int m, unsigned tag,
+                                           unsigned drop, Bars *sb, WsHeader *hdr) {
+    ln.tile(i, T.b, T.c);
+    T.g = T.b * ln.nchunks + T.c;
+    T.Tc = min(T_TOK, L - T.c * T_TOK);
+    T.r = i % REGIONS;
+    if (!pipe_wait(&sb->tmem_full[T.r], (i / REGIONS) & 1, sb, hdr)) return false;
+    tc_fence_after();
+    const uint32_t col0 = lane_base + (uint32_t)T.r * 128u;
     T.elo = make_float2(0.f, 0.f);
-    T.E = (T.Tc == T_TOK) ? pass1_full(col0, x.kc, T.elo) : pass1_short(col0, T.Tc, x.kc.lb);
-    const bool publish = x.drop != (unsigned)(T.tile + 1);
-    float4 *my = x.rec + (size_t)T.tile * P_M + x.m;
-    if (T.c == 0) {
-        T.carry = x.x0 ? x.x0[(size_t)T.b * P_M + x.m] : make_float2(0.f, 0.f);
-        const float2 A = (T.Tc == T_TOK) ? x.kc.lb64 : cpow(x.kc.lb, T.Tc);
-        const float2 inc = cfma(A, T.carry, T.E);
-        if (publish) st_record(my, inc.x, inc.y, 0.f, __uint_as_float(x.incl_word));
-        T.pending = false;
-    } else {
-        if (publish) st_record(my, T.E.x, T.E.y, 0.f, __uint_as_float(x.agg_word));
-        T.pending = true;
-    }
-}
-
-// Issues the first window of look-back loads of a pending tile.
-__device__ __forceinline__ void scan_issue(const ScanCtx &x, const ScanTile &T, float4 (&v)[LB_WIN]) {
-    lb_issue(v, x.rec + (size_t)T.b * P_M + x.m, x.stride, T.c - 1);
-}
-
-// Completes the look-back of a tile and publishes its inclusive state.
-__device__ __forceinline__ void scan_resolve(const ScanCtx &x, ScanTile &T, float4 (&v)[LB_WIN]) {
-    T.carry = lb_finish(v, x.rec + (size_t)T.b * P_M + x.m, x.stride, T.c - 1, x.kc.lb64, x.epoch,
-                        x.hdr, x.limit, T.tile);
-    const float2 A = (T.Tc == T_TOK) ? x.kc.lb64 : cpow(x.kc.lb, T.Tc);
-    const float2 inc = cfma(A, T.carry, T.E);
-    if (x.drop != (unsigned)(T.tile + 1))
-        st_record(x.rec + (size_t)T.tile * P_M + x.m, inc.x, inc.y, 0.f, __uint_as_float(x.incl_word));
-    T.pending = false;
+    const float2 E = (T.Tc == T_TOK) ? pass1_full(col0, kc, T.elo) : pass1_short(col0, T.Tc, kc.lb);
+    if (drop != (unsigned)T.g + 1u) st_record(rec + (size_t)T.g * P_M + m, E, tag);
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -445,141 +428,158 @@ __global__ void weight_images_kernel(const float2 *__restrict__ b_bar, const flo
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(THREADS, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    unsigned char *smem = smem_raw + pad;
     Bars *sb = reinterpret_cast<Bars *>(smem + SM_BAR);
-    __shared__ unsigned s_epoch, s_drop;
-    __shared__ unsigned long long s_limit;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WsHeader *hdr = args.ws.hdr;
-    float4 *rec = args.ws.agg;
-    const int B = args.B, L = args.L;
+    float4 *rec = args.ws.agg;         // [ntiles][P] aggregate records
+    const int B = args.B, L = args.L, nchunks = args.nchunks, W = args.W;
+    Lane ln;
+    ln.B = B;
+    ln.W = W;
+    ln.G = (int)gridDim.x;
+    ln.k = (int)blockIdx.x;
+    ln.nchunks = nchunks;
+    const int n = ln.count();
+    // the allocation must hold the 1024-aligned layout (the same for every thread)
+    const bool fits = pad + SM_TOTAL <= SMEM_REQUEST;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sb->full_u[s], 1);
-            mbar_init(&sb->empty_u[s], 5);   // GEMM1 commit + 4 epilogue warps
+    if (fits) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(&sb->full_u[s], 1);
+                mbar_init(&sb->empty_u[s], 2);   // the two GEMM1 halves
+            }
+            for (int r = 0; r < REGIONS; ++r) {
+                mbar_init(&sb->tmem_full[r], 2);   // the two GEMM1 halves
+                mbar_init(&sb->tmem_empty[r], 4);  // the four epilogue warps
+                mbar_init(&sb->mma2_done[r], 2);   // the two GEMM2 halves
+            }
+            mbar_init(&sb->xready, 4);
+            mbar_init(&sb->xfree, 2);
+            mbar_init(&sb->weights, 1);
+            mbar_init(&sb->drain, 4);          // the four issuing threads
+            for (int q = 0; q < 2; ++q) {
+                mbar_init(&sb->carry_full[q], 4);    // the four fold warps
+                mbar_init(&sb->carry_empty[q], 4);   // the four scan warps
+            }
+            sb->abort = 0;
+            fence_mbar_init();
+            sb->epoch = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
+            sb->drop = *reinterpret_cast<volatile unsigned *>(&hdr->drop_publish);
+            const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
+            sb->limit_ns = 1000ull * (lim ? lim : 1000000u);
         }
-        for (int r = 0; r < REGIONS; ++r) {
-            mbar_init(&sb->tmem_full[r], 1);
-            mbar_init(&sb->tmem_empty[r], 4);
-            mbar_init(&sb->mma2_done[r], 1);
+        if (warp == W_TMEM) {
+            tmem_alloc(&sb->tmem_base, 512);
+            tmem_relinquish();
         }
-        mbar_init(&sb->xready, 4);
-        mbar_init(&sb->xfree, 1);
-        mbar_init(&sb->weights, 1);
-        mbar_init(&sb->drain, 1);
-        sb->n_local = args.ntiles > (int)blockIdx.x
-                          ? (args.ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
-                          : 0;
-        sb->abort = 0;
-        fence_mbar_init();
-        s_epoch = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
-        s_drop = *reinterpret_cast<volatile unsigned *>(&hdr->drop_publish);
-        const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
-        s_limit = 1000ull * (lim ? lim : 1000000u);
-    }
-    if (warp == W_TMEM) {
-        tmem_alloc(&sb->tmem_base, 512);
-        tmem_relinquish();
+    } else if (threadIdx.x == 0) {
+        latch_status(hdr, S5_ERR_UNSUPPORTED);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sb->tmem_base;
-    const unsigned epoch = s_epoch;
+    const uint32_t tmem = fits ? sb->tmem_base : 0u;
+    const unsigned tag = fits ? ((sb->epoch << 2) | FLAG_AGG) : 0u;
 
-    if (warp == W_PROD) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tmap(&tmap_u);
-            mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
-            bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
-            bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
-            int last_issue[STAGES];
-            for (int s = 0; s < STAGES; ++s) last_issue[s] = -1;
-            const int n_local = sb->n_local;
-            for (int i = 0; i < n_local; ++i) {
-                const int s = i % STAGES;
-                if (i >= STAGES && !pipe_wait(&sb->empty_u[s], ((i / STAGES) - 1) & 1, sb, hdr)) break;
-                const int tile = (int)blockIdx.x + i * (int)gridDim.x;
-                const int b = tile % B, c = tile / B;
-                unsigned char *dst = smem + SM_U + s * U_STAGE;
-                mbar_arrive_tx(&sb->full_u[s], U_STAGE);
-                tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
-                tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
-                last_issue[s] = i;
-            }
-            // copies still in flight must land before the CTA exits
-            drain_wait(&sb->weights, 0);
-            for (int s = 0; s < STAGES; ++s)
-                if (last_issue[s] >= 0) drain_wait(&sb->full_u[s], (last_issue[s] / STAGES) & 1);
-        }
-    } else if (warp == W_MMA) {
-        // ------------------------------------------------------------ MMA issuer
+    if (!fits) {
+        // nothing to run: straight to the teardown
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ TMA + MMA issue
+        // One dependent chain of 8 MMAs per thread and tile: a single thread
+        // issues a chain of accumulating MMAs at roughly one per 235 cycles, so
+        // the tile's 32 MMAs are spread over four issuing threads.
+        //   warp 1: GEMM1 rows 0..P-1 (Re),  warp 2: GEMM1 rows P..2P-1 (Im),
+        //   warp 3: GEMM2 k-steps 0..7,      warp 0: GEMM2 k-steps 8..15 and the
+        //   TMA producer.  GEMM2's two halves accumulate into columns 0..63 and
+        //   64..127 of the tile's region; the epilogue adds them.
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, T_TOK);
             const uint32_t bs = smem_addr(smem + SM_BS), cp = smem_addr(smem + SM_CP);
             const uint32_t xs = smem_addr(smem + SM_X);
-            bool ok = pipe_wait(&sb->weights, 0, sb, hdr);
-            int g1 = 0, g2 = 0;          // next tile for GEMM1 / GEMM2
-            const int n_end = sb->n_local;
-            unsigned long long t0 = global_ns();
-            while (ok) {
-                bool progress = false;
-                // GEMM1 of tile g1: u tile landed and its TMEM region is free
-                if (g1 < n_end) {
-                    const int s = g1 % STAGES, r = g1 % REGIONS;
-                    if (mbar_test_wait(&sb->full_u[s], (g1 / STAGES) & 1) &&
-                               (g1 < REGIONS ||
-                                mbar_test_wait(&sb->tmem_empty[r], ((g1 / REGIONS) - 1) & 1))) {
+            if (warp == 0) {
+                prefetch_tmap(&tmap_u);
+                mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
+                bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
+                bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
+            }
+            bool ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
+            if (warp == 1 || warp == 2) {
+                const int mb = warp - 1;
+                for (int g = 0; ok && g < n; ++g) {
+                    const int s = g % STAGES, r = g % REGIONS;
+                    ok = pipe_wait(&sb->full_u[s], (g / STAGES) & 1, sb, hdr) &&
+                         (g < REGIONS || pipe_wait(&sb->tmem_empty[r], ((g / REGIONS) - 1) & 1, sb, hdr));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t ub = smem_addr(smem + SM_U + s * U_STAGE);
+#pragma unroll
+                    for (int kq = 0; kq < H_F / 16; ++kq)
+                        mma_bf16(tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u,
+                                 sw128_kmajor_desc(bs + (kq >> 2) * (2 * P_M * 128) + mb * (P_M * 128) + (kq & 3) * 32),
+                                 sw128_kmajor_desc(ub + (kq >> 2) * (T_TOK * 128) + (kq & 3) * 32), idesc, kq > 0);
+                    mma_commit(&sb->tmem_full[r]);
+                    mma_commit(&sb->empty_u[s]);
+                }
+            } else {
+                // GEMM2 half hf (and, in warp 0, the u loads)
+                const int hf = warp == 3 ? 0 : 1;
+                int g2 = 0, il = 0;   // next tile for GEMM2 / for a u load
+                int last_issue[STAGES];
+                for (int q = 0; q < STAGES; ++q) last_issue[q] = -1;
+                const int nl = warp == 0 ? n : 0;
+                unsigned long long t0 = global_ns();
+                while (ok && (g2 < n || il < nl)) {
+                    bool progress = false;
+                    if (il < nl) {
+                        const int s = il % STAGES;
+                        if (il < STAGES || mbar_test_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1)) {
+                            int b, c;
+                            ln.tile(il, b, c);
+                            unsigned char *dst = smem + SM_U + s * U_STAGE;
+                            mbar_arrive_tx(&sb->full_u[s], U_STAGE);
+                            tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
+                            tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
+                            last_issue[s] = il;
+                            ++il;
+                            progress = true;
+                        }
+                    }
+                    if (g2 < n && mbar_test_wait(&sb->xready, g2 & 1)) {
                         tc_fence_after();
-                        const uint32_t ub = smem_addr(smem + SM_U + s * U_STAGE);
-                        // rolled loops: descriptors are rebuilt per MMA rather than
-                        // hoisted into (many) registers
-#pragma unroll 1
-                        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll 1
-                            for (int k = 0; k < H_F / 16; ++k)
-                                mma_bf16(tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u,
-                                         sw128_kmajor_desc(bs + (k >> 2) * (2 * P_M * 128) +
-                                                           mb * (P_M * 128) + (k & 3) * 32),
-                                         sw128_kmajor_desc(ub + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
-                                         idesc, k > 0);
-                        mma_commit(&sb->tmem_full[r]);
-                        mma_commit(&sb->empty_u[s]);
-                        ++g1;
+                        const uint32_t d = tmem + (uint32_t)(g2 % REGIONS) * 128u + (uint32_t)hf * 64u;
+#pragma unroll
+                        for (int k8 = 0; k8 < 8; ++k8) {
+                            const int kq = hf * 8 + k8;
+                            mma_bf16(d, sw128_kmajor_desc(cp + (kq >> 2) * (H_F * 128) + (kq & 3) * 32),
+                                     sw128_kmajor_desc(xs + (kq >> 2) * (T_TOK * 128) + (kq & 3) * 32), idesc,
+                                     k8 > 0);
+                        }
+                        mma_commit(&sb->mma2_done[g2 % REGIONS]);
+                        mma_commit(&sb->xfree);
+                        ++g2;
                         progress = true;
                     }
+                    if (progress) {
+                        t0 = global_ns();
+                    } else if (aborted(sb)) {
+                        break;
+                    } else if (global_ns() - t0 > PIPE_WAIT_NS) {
+                        set_abort(sb, hdr);
+                        break;
+                    } else {
+                        __nanosleep(32);
+                    }
                 }
-                // GEMM2 of tile g2: its scan wrote X
-                if (g2 < g1 && mbar_test_wait(&sb->xready, g2 & 1)) {
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(g2 % REGIONS) * 128u;
-#pragma unroll 1
-                    for (int k = 0; k < 2 * P_M / 16; ++k)
-                        mma_bf16(d, sw128_kmajor_desc(cp + (k >> 2) * (H_F * 128) + (k & 3) * 32),
-                                 sw128_kmajor_desc(xs + (k >> 2) * (T_TOK * 128) + (k & 3) * 32),
-                                 idesc, k > 0);
-                    mma_commit(&sb->mma2_done[g2 % REGIONS]);
-                    mma_commit(&sb->xfree);
-                    ++g2;
-                    progress = true;
-                }
-                if (g2 >= n_end) break;
-                if (progress) {
-                    t0 = global_ns();
-                } else if (aborted(sb)) {
-                    break;
-                } else if (global_ns() - t0 > PIPE_WAIT_NS) {
-                    set_abort(sb, hdr);
-                    break;
-                } else {
-                    // yield the issue slots of this SM sub-partition to the
-                    // scan and epilogue warps that share it
-                    __nanosleep(64);
+                if (warp == 0) {
+                    // copies still in flight must land before the CTA exits
+                    drain_wait(&sb->weights, 0);
+                    for (int q = 0; q < STAGES; ++q)
+                        if (last_issue[q] >= 0) drain_wait(&sb->full_u[q], (last_issue[q] / STAGES) & 1);
                 }
             }
             // every MMA issued must complete before TMEM is freed
@@ -592,10 +592,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         const int m = 32 * qd + lane;
         ScanConsts kc;
         kc.lb = args.lambda_bar[m];
-        kc.lb8 = cpow(kc.lb, 8);
-        kc.lb16 = cmul(kc.lb8, kc.lb8);
-        kc.lb32 = cmul(kc.lb16, kc.lb16);
+        kc.lb32 = cpow(kc.lb, 32);
         kc.lb64 = cmul(kc.lb32, kc.lb32);
+        const float2 lw1 = cpow(kc.lb64, W - 1);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const uint32_t xcol = (uint32_t)lane * 4u;   // byte of (Re, Im) in this warp's k-block row
         // shared address of (row q, this lane's column) in each swizzle phase q;
@@ -605,135 +604,125 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         for (int q = 0; q < 8; ++q)
             xb[q] = smem_addr(smem + SM_X + qd * (T_TOK * 128)) + 128u * q +
                     ((((xcol >> 4) ^ (uint32_t)q)) << 4) + (xcol & 15u);
-        ScanCtx cx;
-        cx.kc = kc;
-        cx.lane_base = lane_base;
-        cx.rec = rec;
-        cx.x0 = args.x0;
-        cx.stride = (size_t)B * P_M;
-        cx.B = B;
-        cx.L = L;
-        cx.m = m;
-        cx.epoch = epoch;
-        cx.drop = s_drop;
-        cx.agg_word = (epoch << 2) | FLAG_AGG;
-        cx.incl_word = (epoch << 2) | FLAG_INCL;
-        cx.limit = s_limit;
-        cx.hdr = hdr;
-        float4 v[LB_WIN];
-        const int n_local = sb->n_local;
-        // Three tiles in flight: t0 (pass 2 this iteration), t1 (look-back
-        // resolved this iteration, its records' loads issued last iteration),
-        // t2 (pass 1 this iteration).  A tile's look-back therefore runs a full
-        // iteration after every CTA published the aggregates it needs.
+        const float2 *slots = reinterpret_cast<const float2 *>(smem + SM_CARRY);
+        const unsigned drop = sb->drop;
+
+        // Every exit from this loop is decided by named_bar_and, so the four
+        // warps always meet at the same barriers.
         ScanTile t0, t1, t2;
-        auto start = [](ScanTile &T, int i, int B_, int L_) {
-            T.tile = (int)blockIdx.x + i * (int)gridDim.x;
-            T.b = T.tile % B_;
-            T.c = T.tile / B_;
-            T.Tc = min(T_TOK, L_ - T.c * T_TOK);
-            T.r = i % REGIONS;
-        };
-        // pass 1 of local tile i (u landed, D1 ready)
-        bool ok = true;
-#define S5_FRONT(T, I)                                                                     \
-    do {                                                                                   \
-        if (wait_tile((I), sb, hdr) < 0) { ok = false; break; }                            \
-        start((T), (I), B, L);                                                             \
-        if (!pipe_wait(&sb->tmem_full[(T).r], ((I) / REGIONS) & 1, sb, hdr)) { ok = false; break; } \
-        tc_fence_after();                                                                  \
-        scan_front(cx, (T));                                                               \
-    } while (0)
-        if (n_local > 0) {
-            S5_FRONT(t0, 0);
-            if (ok && t0.pending) {
-                scan_issue(cx, t0, v);
-                scan_resolve(cx, t0, v);
-            }
-            if (ok && n_local > 1) {
-                S5_FRONT(t1, 1);
-                if (ok && t1.pending) scan_issue(cx, t1, v);
+        bool alive = true;
+        for (int j = 0; j < 2 && j < n; ++j) {
+            ScanTile &T = j == 0 ? t0 : t1;
+            const bool mine = scan_front(T, j, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
+            if (!named_bar_and(BAR_SCAN, 128, mine)) {
+                alive = false;
+                break;
             }
         }
-        for (int i = 0; ok && i < n_local; ++i) {
-            if (i + 2 < n_local) {
-                S5_FRONT(t2, i + 2);
-                if (!ok) break;
+        float2 xprev = make_float2(0.f, 0.f);
+        bool mine = true;
+        for (int i = 0; alive && i < n; ++i) {
+            const bool front = i + 2 < n;
+            if (mine && front)
+                mine = scan_front(t2, i + 2, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
+            if (!named_bar_and(BAR_SCAN, 128, mine)) break;
+            // carry of tile i: window sum from the fold warps' slot
+            mine = pipe_wait(&sb->carry_full[i & 1], (i >> 1) & 1, sb, hdr);
+            if (mine) {
+                const float2 wsum = slots[(i & 1) * P_M + m];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sb->carry_empty[i & 1]);
+                float2 carry;
+                if (t0.c < W) {
+                    const float2 x0v = args.x0 ? args.x0[(size_t)t0.b * P_M + m] : make_float2(0.f, 0.f);
+                    carry = cfma(cpow(kc.lb64, t0.c), x0v, wsum);
+                } else {
+                    carry = cfma(lw1, xprev, wsum);
+                }
+                // pass 2 of tile i once GEMM2 of tile i-1 has read X
+                mine = i == 0 || pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr);
+                if (mine) {
+                    tc_fence_after();
+                    const uint32_t col0 = lane_base + (uint32_t)t0.r * 128u;
+                    xprev = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, carry, t0.elo)
+                                             : pass2_short(col0, xb, kc.lb, carry, t0.Tc);
+                    if (t0.c == nchunks - 1 && args.x_last) args.x_last[(size_t)t0.b * P_M + m] = xprev;
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sb->xready);
+                }
             }
-            if (i + 1 < n_local && t1.pending) scan_resolve(cx, t1, v);
-            // pass 2 of tile i
-            if (i >= 1 && !pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr)) break;
-            const uint32_t col0 = lane_base + (uint32_t)t0.r * 128u;
-            const float2 xend = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, t0.carry, t0.elo)
-                                                 : pass2_short(col0, xb, kc.lb, t0.carry, t0.Tc);
-            if (t0.c == args.nchunks - 1 && args.x_last) args.x_last[(size_t)t0.b * P_M + m] = xend;
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sb->xready);
-            if (i + 2 < n_local && t2.pending) scan_issue(cx, t2, v);
             t0 = t1;
             t1 = t2;
         }
-#undef S5_FRONT
     } else if (warp >= W_EPI && warp < W_EPI + 4) {
         // ------------------------------------------------------------ epilogue
         const int qd = warp - W_EPI;
         const int h = 32 * qd + lane;
         const float dh = args.d[h];
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        const uint32_t hkb = (uint32_t)h >> 6, hc = (uint32_t)h & 63u;
-        // offset inside a stage of (row q, this feature) in swizzle phase q;
-        // row t lives at ub[t & 7] + (t >> 3) * 1024
-        uint32_t ub[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            ub[q] = hkb * (T_TOK * 128) + 128u * q + (((hc >> 3) ^ (uint32_t)q) << 4) + ((hc & 7u) << 1);
-        const uint32_t stage0 = smem_addr(smem + SM_U);
+        const __nv_bfloat16 *uin = static_cast<const __nv_bfloat16 *>(args.u);
         __nv_bfloat16 *yout = static_cast<__nv_bfloat16 *>(args.y);
-        for (int i = 0;; ++i) {
-            const int tile = wait_tile(i, sb, hdr);
-            if (tile < 0) break;
-            const int s = i % STAGES, r = i % REGIONS;
-            const int b = tile % B, c = tile / B;
+        for (int i = 0; i < n; ++i) {
+            const int r = i % REGIONS;
+            int b, c;
+            ln.tile(i, b, c);
             const int Tc = min(T_TOK, L - c * T_TOK);
+            const size_t row0 = ((size_t)b * L + (size_t)c * T_TOK) * H_F + h;
+            // this feature's u over the tile, loaded before the wait so that
+            // the latency overlaps it
+            __nv_bfloat16 uv[T_TOK];
+#pragma unroll
+            for (int k = 0; k < T_TOK; ++k)
+                uv[k] = (k < Tc) ? uin[row0 + (size_t)k * H_F] : __float2bfloat16_rn(0.f);
             if (!pipe_wait(&sb->mma2_done[r], (i / REGIONS) & 1, sb, hdr)) break;
             tc_fence_after();
-            const uint32_t sbase = stage0 + (uint32_t)s * U_STAGE;
-            __nv_bfloat16 *yrow = yout + ((size_t)b * L + (size_t)c * T_TOK) * H_F + h;
+            __nv_bfloat16 *yrow = yout + row0;
 #pragma unroll
             for (int ch = 0; ch < T_TOK / 16; ++ch) {
-                uint32_t yv[16];
-                tmem_ld16(lane_base + (uint32_t)r * 128u + ch * 16, yv);
+                uint32_t ya[16], yb[16];
+                tmem_ld16(lane_base + (uint32_t)r * 128u + ch * 16, ya);
+                tmem_ld16(lane_base + (uint32_t)r * 128u + 64u + ch * 16, yb);
                 tmem_wait_ld();
+                float yv[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) yv[k] = __uint_as_float(ya[k]) + __uint_as_float(yb[k]);
                 if (ch == 3) {
                     // every column of the region has been read: it may be reused
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sb->tmem_empty[r]);
                 }
-                float uf[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int t = ch * 16 + k;
-                    uf[k] = __uint_as_float(lds16(sbase + ub[t & 7] + (uint32_t)(t >> 3) * 1024u) << 16);
-                }
                 if (Tc == T_TOK) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        yrow[(size_t)(ch * 16 + k) * H_F] =
-                            __float2bfloat16_rn(fmaf(dh, uf[k], __uint_as_float(yv[k])));
+                        yrow[(size_t)(ch * 16 + k) * H_F] = __float2bfloat16_rn(
+                            fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
                 } else {
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         if (ch * 16 + k < Tc)
-                            yrow[(size_t)(ch * 16 + k) * H_F] =
-                                __float2bfloat16_rn(fmaf(dh, uf[k], __uint_as_float(yv[k])));
+                            yrow[(size_t)(ch * 16 + k) * H_F] = __float2bfloat16_rn(
+                                fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
                 }
             }
-            // u has been read: the stage may be refilled
+        }
+    } else if (warp >= W_FOLD && warp < W_FOLD + 4) {
+        // ------------------------------------------------------------ carry windows
+        const int m = 32 * (warp - W_FOLD) + lane;
+        const float2 lam = cpow(args.lambda_bar[m], 64);
+        float2 *slots = reinterpret_cast<float2 *>(smem + SM_CARRY);
+        const unsigned long long limit = sb->limit_ns;
+        bool gave_up = false;
+        for (int j = 0; j < n; ++j) {
+            // slot j % 2 is free once the scan has read tile j-2's sum
+            if (j >= 2 && !pipe_wait(&sb->carry_empty[j & 1], ((j >> 1) - 1) & 1, sb, hdr)) break;
+            int b, c;
+            ln.tile(j, b, c);
+            slots[(j & 1) * P_M + m] = fold_window(rec, b, c, nchunks, W, m, lam, tag, hdr, limit, gave_up);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sb->empty_u[s]);
+            if (lane == 0) mbar_arrive(&sb->carry_full[j & 1]);
         }
     }
 
@@ -741,14 +730,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == W_TMEM) tmem_dealloc(tmem, 512);
+    if (fits && warp == W_TMEM) tmem_dealloc(tmem, 512);
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&hdr->done_counter, 1u);
         if (prev == gridDim.x - 1) {
+            const unsigned e = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
             hdr->tile_counter = 0;
             hdr->done_counter = 0;
-            hdr->epoch = (s_epoch + 1) & 0x3FFFFFFFu;
+            hdr->epoch = (e + 1) & 0x3FFFFFFFu;
             __threadfence();
         }
     }
@@ -788,7 +778,26 @@ bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16) {
     return H == H_F && P == P_M && u_bf16 && y_bf16 && proj_bf16;
 }
 
-cudaError_t launch_forward_tc(const TcArgs &a, const void *u, cudaStream_t st, int num_sms) {
+// Lanes per sequence and grid: B * W CTAs (W <= nchunks, W <= W_MAX) when the
+// sequences fit on the SMs, else W = 1 and one CTA per SM.
+void tc_grid(int B, int nchunks, int num_sms, int *W, int *G) {
+    if (B <= num_sms) {
+        int w = num_sms / B;
+        if (w > nchunks) w = nchunks;
+        if (w > W_MAX) w = W_MAX;
+        *W = w;
+        *G = B * w;
+    } else {
+        *W = 1;
+        *G = num_sms;
+    }
+}
+
+cudaError_t launch_forward_tc(const TcArgs &a0, const void *u, cudaStream_t st, int num_sms) {
+    TcArgs a = a0;
+    a.u = u;
+    int G = 0;
+    tc_grid(a.B, a.nchunks, num_sms, &a.W, &G);
     CUtensorMap mu;
     if (!make_map(&mu, u, a.B, a.L)) return cudaErrorInvalidValue;
     const int words = P_M * H_F / 2 + H_F * P_M;
@@ -798,15 +807,14 @@ cudaError_t launch_forward_tc(const TcArgs &a, const void *u, cudaStream_t st, i
     e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_REQUEST);
     if (e != cudaSuccess) return e;
-    // Cooperative launch: one CTA per SM, all resident, so the static wave
-    // assignment never waits on a CTA that has not started.
+    // Cooperative launch: one CTA per SM, all resident, so a lane never waits
+    // on a CTA that has not started.
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_tc_kernel, THREADS, SMEM_REQUEST);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    const int grid = num_sms < a.ntiles ? num_sms : a.ntiles;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_REQUEST;
     cfg.stream = st;

@@ -14,8 +14,10 @@ struct TcArgs {
     void *y;                   // [B][L][H] bf16
     const float2 *x0;          // [B][P] or null
     float2 *x_last;            // [B][P] or null
+    const void *u;             // [B][L][H] bf16 (set by launch_forward_tc)
     int B, L, nchunks, ntiles;
-    WsLayout ws;               // per-mode carry records live in ws.agg
+    int W;                     // lanes per sequence (set by launch_forward_tc)
+    WsLayout ws;               // aggregate records: values in ws.incl, flags in ws.flags
 };
 
 // The tensor-core kernel covers H = 128, P = 128 with bf16 u, y and projections.
