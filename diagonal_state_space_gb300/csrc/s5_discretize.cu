@@ -10,8 +10,7 @@
 // The per-mode factors are computed in float64 (only P values per call) with
 // a complex expm1, e^z - 1 = expm1(x)cos(y) - 2 sin^2(y/2) + i e^x sin(y), so
 // that small |z| loses no digits; below |z| = 1e-4 a Taylor series of phi1 is
-// used instead, as the review's reference does.  One block per mode; thread 0
-// computes the mode's factor, every thread scales a slice of the B_tilde row.
+// used instead, as the review's reference does.
 #include "s5_internal.cuh"
 
 namespace s5 {
@@ -26,55 +25,71 @@ __device__ inline dcplx ddiv(dcplx a, dcplx b) {
     return {(a.re * b.re + a.im * b.im) / den, (a.im * b.re - a.re * b.im) / den};
 }
 
-// (e^z - 1)/lambda for z = lambda*dt, and e^z.
-__device__ inline void zoh_factors(dcplx lam, double dt, dcplx *abar, dcplx *gain) {
-    dcplx z = {lam.re * dt, lam.im * dt};
-    double s, c;
-    sincos(z.im, &s, &c);
-    double mag = exp(z.re);
-    *abar = {mag * c, mag * s};
-    double zabs = sqrt(z.re * z.re + z.im * z.im);
-    if (zabs < 1e-4) {
-        // dt * (1 + z/2 + z^2/6 + z^3/24 + z^4/120); the next term is below 1e-22.
-        dcplx term = {1.0, 0.0}, phi = {1.0, 0.0};
-        for (int n = 1; n <= 4; ++n) {
-            term = dmul(term, z);
-            double f = 1.0 / (double)(n + 1);
-            term.re *= f;
-            term.im *= f;
-            phi.re += term.re;
-            phi.im += term.im;
-        }
-        *gain = {dt * phi.re, dt * phi.im};
-    } else {
-        double sh = sin(0.5 * z.im);
-        dcplx em1 = {expm1(z.re) * c - 2.0 * sh * sh, mag * s};
-        *gain = ddiv(em1, lam);
-    }
-}
-
+// One block per mode (float64 throughput per SM is small, so the work is
+// spread over P SMs).  The float64 functions of the mode's factors are spread
+// over the first four threads, so that each evaluates at most two of them in
+// sequence:
+//   every thread  dt = exp(log_dt)
+//   thread 0      sin(Im z), cos(Im z)      thread 1  exp(Re z)
+//   thread 2      expm1(Re z)               thread 3  sin(Im z / 2)
+// then lambda_bar = e^Re z (cos, sin) and, for |z| >= 1e-4,
+// (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z))/lambda;
+// below |z| = 1e-4, Delta * phi1(z) from its Taylor series.  Every thread of
+// the block then scales a slice of the B_tilde row.
 __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float *__restrict__ log_dt,
                                   const float2 *__restrict__ b_tilde, int P, int H,
                                   float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar) {
     const int p = blockIdx.x;
     __shared__ double s_gain[2];
-    if (threadIdx.x == 0) {
-        float2 l = lambda[p];
-        dcplx lam = {(double)l.x, (double)l.y};
-        double dt = exp((double)log_dt[p]);
-        dcplx abar, gain;
-        zoh_factors(lam, dt, &abar, &gain);
-        lambda_bar[p] = make_float2((float)abar.re, (float)abar.im);
-        s_gain[0] = gain.re;
-        s_gain[1] = gain.im;
+    if (threadIdx.x < 32) {
+        const int q = threadIdx.x & 3;
+        const float2 l = lambda[p];
+        const dcplx lam = {(double)l.x, (double)l.y};
+        const double dt = exp((double)log_dt[p]);
+        const dcplx z = {lam.re * dt, lam.im * dt};
+        double f0 = 0.0, f1 = 0.0;
+        if (threadIdx.x < 4) {
+            if (q == 0) sincos(z.im, &f0, &f1);
+            else if (q == 1) f0 = exp(z.re);
+            else if (q == 2) f0 = expm1(z.re);
+            else f0 = sin(0.5 * z.im);
+        }
+        const unsigned full = 0xffffffffu;
+        const double s = __shfl_sync(full, f0, 0), c = __shfl_sync(full, f1, 0);
+        const double mag = __shfl_sync(full, f0, 1);
+        const double em1r = __shfl_sync(full, f0, 2);
+        const double sh = __shfl_sync(full, f0, 3);
+        if (threadIdx.x == 0) {
+            dcplx gain;
+            const double zabs = sqrt(z.re * z.re + z.im * z.im);
+            if (zabs < 1e-4) {
+                // dt * (1 + z/2 + z^2/6 + z^3/24 + z^4/120); the next term is below 1e-22.
+                dcplx term = {1.0, 0.0}, phi = {1.0, 0.0};
+                for (int n = 1; n <= 4; ++n) {
+                    term = dmul(term, z);
+                    const double f = 1.0 / (double)(n + 1);
+                    term.re *= f;
+                    term.im *= f;
+                    phi.re += term.re;
+                    phi.im += term.im;
+                }
+                gain = {dt * phi.re, dt * phi.im};
+            } else {
+                const dcplx em1 = {em1r * c - 2.0 * sh * sh, mag * s};
+                gain = ddiv(em1, lam);
+            }
+            lambda_bar[p] = make_float2((float)(mag * c), (float)(mag * s));
+            s_gain[0] = gain.re;
+            s_gain[1] = gain.im;
+        }
     }
     __syncthreads();
     const dcplx g = {s_gain[0], s_gain[1]};
     const float2 *src = b_tilde + (size_t)p * H;
     float2 *dst = b_bar + (size_t)p * H;
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        float2 bt = src[h];
-        dcplx v = dmul(g, dcplx{(double)bt.x, (double)bt.y});
+        const float2 bt = src[h];
+        const dcplx v = dmul(g, dcplx{(double)bt.x, (double)bt.y});
         dst[h] = make_float2((float)v.re, (float)v.im);
     }
 }
@@ -103,7 +118,7 @@ __global__ void mode_consts_kernel(const float2 *__restrict__ lambda, const floa
 
 cudaError_t launch_discretize(const float2 *lambda, const float *log_dt, const float2 *b_tilde,
                               int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st) {
-    int threads = H >= 256 ? 256 : (H >= 128 ? 128 : 64);
+    const int threads = H >= 256 ? 256 : (H >= 128 ? 128 : 64);
     discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar);
     return cudaGetLastError();
 }
