@@ -13,7 +13,7 @@ STATUS = {0: "S5_OK", 1: "S5_ERR_INVALID_ARGUMENT", 2: "S5_ERR_UNSUPPORTED", 3: 
           4: "S5_ERR_TIMEOUT", 5: "S5_ERR_NONFINITE"}
 
 # Every exported entry point of include/s5.h: name -> (restype, argtypes)
-_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
 SIGNATURES = {
     "s5_discretize": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp]),
     "s5_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp,
@@ -26,6 +26,16 @@ SIGNATURES = {
     "s5_sync_status": (_i, [_vp, _vp]),
     "s5_status_string": (ctypes.c_char_p, [_i]),
     "s5_last_cuda_error": (ctypes.c_char_p, []),
+    # layer stack
+    "s5_stack_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "s5_stack_last_error": (ctypes.c_char_p, []),
+    "s5_layernorm": (_i, [_vp, _vp, _vp, _ll, _i, _vp]),
+    "s5_stack_weights": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "s5_ssm_forward_states": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp,
+                                   _vp, _vp, _sz, _vp]),
+    "s5_gate_residual": (_i, [_vp, _vp, _vp, _vp, _vp, _ll, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "s5_gate_backward": (_i, [_vp, _vp, _vp, _vp, _ll, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "s5_ssm_backward": (_i, [_vp] * 16 + [_i] * 4 + [_vp] * 7 + [_sz, _vp]),
 }
 
 _lock = threading.Lock()
@@ -62,5 +72,10 @@ def check(fn: str, code: int) -> None:
     if code != 0:
         detail = ""
         if code == 3:
-            detail = lib().s5_last_cuda_error().decode()
+            getter = lib().s5_stack_last_error if fn in STACK_FUNCTIONS else lib().s5_last_cuda_error
+            detail = getter().decode()
         raise S5Error(fn, code, detail)
+
+
+STACK_FUNCTIONS = {"s5_layernorm", "s5_stack_weights", "s5_ssm_forward_states", "s5_gate_residual",
+                   "s5_gate_backward", "s5_ssm_backward"}

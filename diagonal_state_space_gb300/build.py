@@ -25,6 +25,13 @@ NVCC_FLAGS = [
 ]
 
 
+# cuBLAS (the stack's plain bf16 GEMMs), found at run time through the
+# toolkit's library directory.
+_CUDA_LIB = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(
+    shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))), "lib64")
+LINK_LIBS = ["-L" + _CUDA_LIB, "-lcublas", "-Xlinker", "-rpath," + _CUDA_LIB]
+
+
 def _nvcc() -> str:
     for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
         if cand and os.path.exists(cand):
@@ -69,7 +76,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if force or _stale(LIB, objs):
         tmp = LIB + ".tmp%d" % os.getpid()
         cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-cudart", "static",
-               "-o", tmp, *objs]
+               "-o", tmp, *objs, *LINK_LIBS]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))

@@ -1,0 +1,701 @@
+// s5_stack.cu -- the layer stack around the S5 layer and its backward, for
+// general shapes (the deep-stack workload: H = 512, P = 256): pre-LayerNorm,
+// the S5 layer with its states kept for the backward, the gated activation,
+// the residual, and the reverse-time adjoint of the whole layer.
+//
+// Sources: "SIMPLIFIED STATE SPACE LAYERS FOR SEQUENCE MODELING" section 6
+// (pre-norm layers), the wiki "Method" step 4 and its pseudocode (hidden =
+// GELU(y), out = hidden * sigmoid(W hidden), no bias per "Paper vs code"), the
+// review's row 4 (residual in the wrapper).  The backward is not on the pages:
+// it is the chain rule of that forward, with the complex-gradient convention
+// grad(z) = dL/dRe z + i dL/dIm z:
+//   x_hat_k = 2 C~^H ybar_k,  s_k = x_hat_k + conj(lambda_bar) s_{k+1},
+//   zbar_k = Re(B_bar^H s_k) + D ybar_k,  dB_bar = sum_k s_k z_k^T,
+//   dC~ = 2 sum_k ybar_k x_k^H,  dD = sum_k ybar_k z_k,
+//   dlambda_bar = sum_k conj(x_{k-1}) s_k,
+// then the zero-order hold's chain rule to lambda, log_dt and B~.
+//
+// Dense contractions (B_bar z, C' X, W h and the weight gradients) are plain
+// bf16 GEMMs with fp32 accumulation, run by cuBLAS; every other step is a
+// kernel of this file.  Scans are complex fp32.
+#include <cublas_v2.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "s5_internal.cuh"
+
+namespace s5 {
+namespace {
+
+constexpr float LN_EPS = 1e-5f;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// GELU (exact erf form) and its derivative; sigmoid.
+__device__ __forceinline__ float gelu(float v) { return 0.5f * v * (1.f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad(float v) {
+    const float cdf = 0.5f * (1.f + erff(v * 0.70710678118654752f));
+    const float pdf = 0.39894228040143268f * expf(-0.5f * v * v);
+    return cdf + v * pdf;
+}
+__device__ __forceinline__ float sigmoid(float v) { return 1.f / (1.f + expf(-v)); }
+
+// ---------------------------------------------------------------------------
+// a6: LayerNorm over the last axis, no affine, biased variance, eps 1e-5.
+// One warp per row; the row is held in registers (H <= 32 * LN_MAXV).
+// ---------------------------------------------------------------------------
+constexpr int LN_MAXV = 32;
+
+__global__ void ln_fwd_kernel(const float *__restrict__ x, float *__restrict__ z,
+                              __nv_bfloat16 *__restrict__ z16, long long N, int H) {
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const float *xr = x + row * H;
+    float v[LN_MAXV];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < LN_MAXV; ++i) {
+        const int h = lane + 32 * i;
+        v[i] = h < H ? xr[h] : 0.f;
+        s += v[i];
+    }
+    const float mean = warp_sum(s) / (float)H;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < LN_MAXV; ++i) {
+        const int h = lane + 32 * i;
+        const float dv = h < H ? v[i] - mean : 0.f;
+        q += dv * dv;
+    }
+    const float inv = 1.f / sqrtf(warp_sum(q) / (float)H + LN_EPS);
+#pragma unroll
+    for (int i = 0; i < LN_MAXV; ++i) {
+        const int h = lane + 32 * i;
+        if (h < H) {
+            const float zv = (v[i] - mean) * inv;
+            z[row * H + h] = zv;
+            if (z16) z16[row * H + h] = __float2bfloat16_rn(zv);
+        }
+    }
+}
+
+// xbar_out = xbar_in + LN'(x)^T zbar with zbar = zg + d * ybar:
+//   xbar += inv * (zbar - mean(zbar) - z * mean(zbar * z)).
+// Each block also sums ybar * z over its rows per column (the partial of
+// dD), written to dd_part[blockIdx.x][H].
+__global__ void ln_bwd_kernel(const float *__restrict__ x, const float *__restrict__ zg,
+                              const float *__restrict__ ybar, const float *__restrict__ d,
+                              const float *xbar_in, float *xbar_out,
+                              float *__restrict__ dd_part, long long N, int H) {
+    extern __shared__ float s_dd[];   // [warps][H]
+    const int warps = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float ddacc[LN_MAXV];
+#pragma unroll
+    for (int i = 0; i < LN_MAXV; ++i) ddacc[i] = 0.f;
+    for (long long row = (long long)blockIdx.x * warps + wid; row < N; row += (long long)gridDim.x * warps) {
+        const float *xr = x + row * H;
+        float v[LN_MAXV];
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < LN_MAXV; ++i) {
+            const int h = lane + 32 * i;
+            v[i] = h < H ? xr[h] : 0.f;
+            s += v[i];
+        }
+        const float mean = warp_sum(s) / (float)H;
+        float q = 0.f;
+#pragma unroll
+        for (int i = 0; i < LN_MAXV; ++i) {
+            const int h = lane + 32 * i;
+            const float dv = h < H ? v[i] - mean : 0.f;
+            q += dv * dv;
+        }
+        const float inv = 1.f / sqrtf(warp_sum(q) / (float)H + LN_EPS);
+        float zb[LN_MAXV];
+        float m1 = 0.f, m2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < LN_MAXV; ++i) {
+            const int h = lane + 32 * i;
+            if (h < H) {
+                const float zv = (v[i] - mean) * inv;
+                const float yb = ybar[row * H + h];
+                ddacc[i] = fmaf(yb, zv, ddacc[i]);
+                zb[i] = fmaf(d[h], yb, zg[row * H + h]);
+                v[i] = zv;
+                m1 += zb[i];
+                m2 += zb[i] * zv;
+            } else {
+                zb[i] = 0.f;
+            }
+        }
+        m1 = warp_sum(m1) / (float)H;
+        m2 = warp_sum(m2) / (float)H;
+#pragma unroll
+        for (int i = 0; i < LN_MAXV; ++i) {
+            const int h = lane + 32 * i;
+            if (h < H) xbar_out[row * H + h] = xbar_in[row * H + h] + inv * (zb[i] - m1 - v[i] * m2);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < LN_MAXV; ++i) {
+        const int h = lane + 32 * i;
+        if (h < H) s_dd[wid * H + h] = ddacc[i];
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        float t = 0.f;
+        for (int w = 0; w < warps; ++w) t += s_dd[w * H + h];
+        dd_part[(size_t)blockIdx.x * H + h] = t;
+    }
+}
+
+// out[h] = sum_b part[b][h]  (fixed order: deterministic)
+__global__ void sum_rows_kernel(const float *__restrict__ part, int nb, int H, float *__restrict__ out) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    float t = 0.f;
+    for (int b = 0; b < nb; ++b) t += part[(size_t)b * H + h];
+    out[h] = t;
+}
+
+// ---------------------------------------------------------------------------
+// a7 + a8: gated activation and residual, elementwise parts.
+// ---------------------------------------------------------------------------
+// y = yg + d * z (the readout's D term), h = GELU(y) as the bf16 GEMM operand.
+__global__ void gate_pre_kernel(const float *__restrict__ yg, const float *__restrict__ z,
+                                const float *__restrict__ d, float *__restrict__ y,
+                                __nv_bfloat16 *__restrict__ h16, long long n, int H) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const float yv = fmaf(d[i % H], z[i], yg[i]);
+        y[i] = yv;
+        h16[i] = __float2bfloat16_rn(gelu(yv));
+    }
+}
+// u_next = u + GELU(y) * sigmoid(a)
+__global__ void gate_post_kernel(const float *__restrict__ u, const float *__restrict__ y,
+                                 const float *__restrict__ a, float *__restrict__ u_next, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        u_next[i] = u[i] + gelu(y[i]) * sigmoid(a[i]);
+}
+// act = ubar * h * s(1-s) (dL/da), ydir = ubar * s (direct part of dL/dh),
+// h16 = GELU(y) as the dW GEMM operand.
+__global__ void gate_bwd_pre_kernel(const float *__restrict__ ubar, const float *__restrict__ y,
+                                    const float *__restrict__ a, __nv_bfloat16 *__restrict__ act16,
+                                    float *__restrict__ ydir, __nv_bfloat16 *__restrict__ h16, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const float hv = gelu(y[i]), sg = sigmoid(a[i]), ub = ubar[i];
+        act16[i] = __float2bfloat16_rn(ub * hv * sg * (1.f - sg));
+        ydir[i] = ub * sg;
+        h16[i] = __float2bfloat16_rn(hv);
+    }
+}
+// ybar = (ydir + W^T act) * GELU'(y), fp32 and bf16.
+__global__ void gate_bwd_post_kernel(const float *__restrict__ ydir, const float *__restrict__ wact,
+                                     const float *__restrict__ y, float *__restrict__ ybar,
+                                     __nv_bfloat16 *__restrict__ ybar16, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const float g = (ydir[i] + wact[i]) * gelu_grad(y[i]);
+        ybar[i] = g;
+        ybar16[i] = __float2bfloat16_rn(g);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 operand images of one layer's weights.
+//   bs [2P][H]: rows 0..P-1 Re B_bar, rows P..2P-1 Im B_bar
+//   cp [H][2P]: (2 Re C~, -2 Im C~) interleaved per mode (readout, K = 2P)
+//   cx [H][2P]: [2 Re C~ | -2 Im C~] halves (x_hat = 2 C~^H ybar)
+//   w16 [H][H]
+// ---------------------------------------------------------------------------
+__global__ void stack_weights_kernel(const float2 *__restrict__ b_bar, const float2 *__restrict__ c_tilde,
+                                     const float *__restrict__ W, int H, int P,
+                                     __nv_bfloat16 *__restrict__ bs, __nv_bfloat16 *__restrict__ cp,
+                                     __nv_bfloat16 *__restrict__ cx, __nv_bfloat16 *__restrict__ w16) {
+    const long long PH = (long long)P * H, HH = (long long)H * H;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * PH + HH;
+         i += (long long)gridDim.x * blockDim.x) {
+        if (i < PH) {
+            const float2 v = b_bar[i];   // [p][h]
+            const long long p = i / H, h = i % H;
+            bs[p * H + h] = __float2bfloat16_rn(v.x);
+            bs[(P + p) * H + h] = __float2bfloat16_rn(v.y);
+        } else if (i < 2 * PH) {
+            const long long k = i - PH;   // [h][p]
+            const long long h = k / P, p = k % P;
+            const float2 c = c_tilde[k];
+            cp[h * 2 * P + 2 * p] = __float2bfloat16_rn(2.f * c.x);
+            cp[h * 2 * P + 2 * p + 1] = __float2bfloat16_rn(-2.f * c.y);
+            cx[h * 2 * P + p] = __float2bfloat16_rn(2.f * c.x);
+            cx[h * 2 * P + P + p] = __float2bfloat16_rn(-2.f * c.y);
+        } else {
+            const long long k = i - 2 * PH;
+            w16[k] = __float2bfloat16_rn(W[k]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// a4 with states kept: x_k = lambda_bar x_{k-1} + Bu_k per sequence and mode.
+// Bu [T][2P] fp32 halves (Re | Im).  Writes x [T][P] (complex fp32) and
+// X [T][2P] bf16 interleaved (Re, Im) as the readout's GEMM operand.  One
+// thread per (sequence, mode), tokens in order; loads run SCAN_U tokens ahead.
+// ---------------------------------------------------------------------------
+constexpr int SCAN_U = 8;
+constexpr int SCAN_THREADS = 32;
+
+__global__ void scan_fwd_kernel(const float *__restrict__ Bu, const float2 *__restrict__ lambda_bar,
+                                const float2 *__restrict__ x0, int L, int P, float2 *__restrict__ x,
+                                __nv_bfloat162 *__restrict__ X) {
+    const int b = blockIdx.y, p = blockIdx.x * SCAN_THREADS + threadIdx.x;
+    if (p >= P) return;
+    const float2 lb = lambda_bar[p];
+    float2 s = x0 ? x0[(size_t)b * P + p] : make_float2(0.f, 0.f);
+    const size_t P2 = 2 * (size_t)P;
+    const float *bu = Bu + (size_t)b * L * P2;
+    float2 *xo = x + (size_t)b * L * P;
+    __nv_bfloat162 *Xo = X + (size_t)b * L * P;
+    for (int k0 = 0; k0 < L; k0 += SCAN_U) {
+        float re[SCAN_U], im[SCAN_U];
+#pragma unroll
+        for (int j = 0; j < SCAN_U; ++j) {
+            const int k = k0 + j;
+            re[j] = k < L ? bu[(size_t)k * P2 + p] : 0.f;
+            im[j] = k < L ? bu[(size_t)k * P2 + P + p] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < SCAN_U; ++j) {
+            const int k = k0 + j;
+            if (k < L) {
+                s = cfma(lb, s, make_float2(re[j], im[j]));
+                xo[(size_t)k * P + p] = s;
+                Xo[(size_t)k * P + p] = __floats2bfloat162_rn(s.x, s.y);
+            }
+        }
+    }
+}
+
+// Reverse-time adjoint: s_k = x_hat_k + conj(lambda_bar) s_{k+1}, from
+// x_hat [T][2P] fp32 halves; writes S [T][2P] bf16 halves (the GEMM operand of
+// zbar and dB_bar) and the per-sequence partial of dlambda_bar,
+// sum_k conj(x_{k-1}) s_k (x_{-1} = x0), to dlam_part[b][p].
+__global__ void scan_bwd_kernel(const float *__restrict__ xhat, const float2 *__restrict__ lambda_bar,
+                                const float2 *__restrict__ x, const float2 *__restrict__ x0, int L, int P,
+                                __nv_bfloat16 *__restrict__ S, float2 *__restrict__ dlam_part) {
+    const int b = blockIdx.y, p = blockIdx.x * SCAN_THREADS + threadIdx.x;
+    if (p >= P) return;
+    const float2 lb = lambda_bar[p];
+    const float2 lc = make_float2(lb.x, -lb.y);
+    const size_t P2 = 2 * (size_t)P;
+    const float *xh = xhat + (size_t)b * L * P2;
+    const float2 *xs = x + (size_t)b * L * P;
+    __nv_bfloat16 *So = S + (size_t)b * L * P2;
+    const float2 xinit = x0 ? x0[(size_t)b * P + p] : make_float2(0.f, 0.f);
+    float2 s = make_float2(0.f, 0.f), acc = make_float2(0.f, 0.f);
+    for (int k0 = L - 1; k0 >= 0; k0 -= SCAN_U) {
+        float re[SCAN_U], im[SCAN_U];
+        float2 xp[SCAN_U];
+#pragma unroll
+        for (int j = 0; j < SCAN_U; ++j) {
+            const int k = k0 - j;
+            re[j] = k >= 0 ? xh[(size_t)k * P2 + p] : 0.f;
+            im[j] = k >= 0 ? xh[(size_t)k * P2 + P + p] : 0.f;
+            xp[j] = k > 0 ? xs[(size_t)(k - 1) * P + p] : xinit;
+        }
+#pragma unroll
+        for (int j = 0; j < SCAN_U; ++j) {
+            const int k = k0 - j;
+            if (k >= 0) {
+                s = cfma(lc, s, make_float2(re[j], im[j]));
+                So[(size_t)k * P2 + p] = __float2bfloat16_rn(s.x);
+                So[(size_t)k * P2 + P + p] = __float2bfloat16_rn(s.y);
+                // conj(x_{k-1}) * s_k
+                acc.x = fmaf(xp[j].x, s.x, fmaf(xp[j].y, s.y, acc.x));
+                acc.y = fmaf(xp[j].x, s.y, fmaf(-xp[j].y, s.x, acc.y));
+            }
+        }
+    }
+    dlam_part[(size_t)b * P + p] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Zero-order hold chain rule (float64), one block per mode:
+//   dB~ = conj(gain) dB_bar,  gphi = sum_h dB_bar conj(B~),
+//   dlambda = conj(dt e^z) dlambda_bar + conj(d gain/d lambda) gphi,
+//   dlog_dt = dt (Re(conj(dlambda_bar) lambda e^z) + Re(conj(gphi) e^z)),
+// with gain = (e^z - 1)/lambda, d gain/d lambda = (dt e^z - gain)/lambda, and
+// for |z| < 1e-4 gain = dt phi1(z), d gain/d lambda = dt^2 phi1'(z) (series).
+// dlambda_bar is the sum of the per-sequence partials; dB_bar comes from the
+// GEMM as [2P][H] (Re rows, then Im rows).
+// ---------------------------------------------------------------------------
+struct dc { double re, im; };
+__device__ __forceinline__ dc dc_mul(dc a, dc b) { return {a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re}; }
+__device__ __forceinline__ dc dc_conj(dc a) { return {a.re, -a.im}; }
+__device__ __forceinline__ dc dc_div(dc a, dc b) {
+    const double den = b.re * b.re + b.im * b.im;
+    return {(a.re * b.re + a.im * b.im) / den, (a.im * b.re - a.re * b.im) / den};
+}
+
+__global__ void zoh_chain_kernel(const float2 *__restrict__ lambda, const float *__restrict__ log_dt,
+                                 const float2 *__restrict__ b_tilde, const float *__restrict__ dbbar,
+                                 const float2 *__restrict__ dlam_part, int B, int H, int P,
+                                 float2 *__restrict__ dlambda, float *__restrict__ dlog_dt,
+                                 float2 *__restrict__ db_tilde) {
+    const int p = blockIdx.x;
+    __shared__ dc s_gain, s_red[32];
+    __shared__ dc s_gphi;
+    const float2 l = lambda[p];
+    const dc lam = {(double)l.x, (double)l.y};
+    const double dt = exp((double)log_dt[p]);
+    const dc z = {lam.re * dt, lam.im * dt};
+    if (threadIdx.x == 0) {
+        const double zabs = sqrt(z.re * z.re + z.im * z.im);
+        double sn, cs;
+        sincos(z.im, &sn, &cs);
+        const double mag = exp(z.re);
+        if (zabs < 1e-4) {
+            dc term = {1.0, 0.0}, phi = {1.0, 0.0};
+            for (int n = 1; n <= 8; ++n) {
+                term = dc_mul(term, z);
+                double f = 1.0;
+                for (int q = 2; q <= n + 1; ++q) f *= (double)q;
+                phi.re += term.re / f;
+                phi.im += term.im / f;
+            }
+            s_gain = {dt * phi.re, dt * phi.im};
+        } else {
+            const double sh = sin(0.5 * z.im);
+            const dc em1 = {expm1(z.re) * cs - 2.0 * sh * sh, mag * sn};
+            s_gain = dc_div(em1, lam);
+        }
+    }
+    __syncthreads();
+    const dc gain = s_gain;
+    // gphi = sum_h dB_bar[p][h] conj(B~[p][h]); dB~ = conj(gain) dB_bar
+    dc part = {0.0, 0.0};
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        const dc g = {(double)dbbar[(size_t)p * H + h], (double)dbbar[(size_t)(P + p) * H + h]};
+        const float2 bt = b_tilde[(size_t)p * H + h];
+        const dc t = dc_mul(g, dc{(double)bt.x, -(double)bt.y});
+        part.re += t.re;
+        part.im += t.im;
+        const dc o = dc_mul(dc_conj(gain), g);
+        db_tilde[(size_t)p * H + h] = make_float2((float)o.re, (float)o.im);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        part.re += __shfl_xor_sync(0xffffffffu, part.re, o);
+        part.im += __shfl_xor_sync(0xffffffffu, part.im, o);
+    }
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        dc gp = {0.0, 0.0};
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            gp.re += s_red[w].re;
+            gp.im += s_red[w].im;
+        }
+        s_gphi = gp;
+        dc gl = {0.0, 0.0};
+        for (int b = 0; b < B; ++b) {
+            const float2 v = dlam_part[(size_t)b * P + p];
+            gl.re += v.x;
+            gl.im += v.y;
+        }
+        double sn, cs;
+        sincos(z.im, &sn, &cs);
+        const double mag = exp(z.re);
+        const dc ab = {mag * cs, mag * sn};
+        const double zabs = sqrt(z.re * z.re + z.im * z.im);
+        dc dg;
+        if (zabs < 1e-4) {
+            // phi1'(z) = sum_{n>=1} n z^(n-1) / (n+1)!
+            dc term = {1.0, 0.0}, sum = {0.0, 0.0};
+            double fact = 2.0;
+            for (int n = 1; n <= 8; ++n) {
+                sum.re += (double)n * term.re / fact;
+                sum.im += (double)n * term.im / fact;
+                term = dc_mul(term, z);
+                fact *= (double)(n + 2);
+            }
+            dg = {dt * dt * sum.re, dt * dt * sum.im};
+        } else {
+            dg = dc_div(dc{dt * ab.re - gain.re, dt * ab.im - gain.im}, lam);
+        }
+        const dc t1 = dc_mul(dc_conj(dc{dt * ab.re, dt * ab.im}), gl);
+        const dc t2 = dc_mul(dc_conj(dg), gp);
+        dlambda[p] = make_float2((float)(t1.re + t2.re), (float)(t1.im + t2.im));
+        const dc la = dc_mul(lam, ab);
+        const double gdt = (gl.re * la.re + gl.im * la.im) + (gp.re * ab.re + gp.im * ab.im);
+        dlog_dt[p] = (float)(dt * gdt);
+    }
+}
+
+// dC~[h][p] = 2 (G[h][2p] - i G[h][2p+1]) from G = ybar^T X.
+__global__ void dc_finish_kernel(const float *__restrict__ g, int H, int P, float2 *__restrict__ dc_tilde) {
+    const long long n = (long long)H * P;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const long long h = i / P, p = i % P;
+        dc_tilde[i] = make_float2(2.f * g[h * 2 * P + 2 * p], -2.f * g[h * 2 * P + 2 * p + 1]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// cuBLAS: one handle per device, used under a lock (the stream is set per call).
+// Row-major C[M][N] = op(A) op(B) with bf16 operands, fp32 accumulation and
+// output: column-major cuBLAS computes C^T = op(B)^T op(A)^T.
+// ---------------------------------------------------------------------------
+std::mutex g_blas_mu;
+cublasHandle_t g_blas[64] = {nullptr};
+
+cublasStatus_t gemm_rm(cudaStream_t st, bool ta, bool tb, int M, int N, int K, const void *A, int lda,
+                       const void *B, int ldb, float *C, int ldc, float alpha = 1.f, float beta = 0.f) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CUBLAS_STATUS_NOT_INITIALIZED;
+    std::lock_guard<std::mutex> lk(g_blas_mu);
+    if (!g_blas[dev]) {
+        cublasStatus_t s = cublasCreate(&g_blas[dev]);
+        if (s != CUBLAS_STATUS_SUCCESS) return s;
+    }
+    cublasHandle_t h = g_blas[dev];
+    cublasStatus_t s = cublasSetStream(h, st);
+    if (s != CUBLAS_STATUS_SUCCESS) return s;
+    return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K, &alpha, B,
+                        CUDA_R_16BF, ldb, A, CUDA_R_16BF, lda, &beta, C, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F,
+                        CUBLAS_GEMM_DEFAULT);
+}
+
+int grid_for(long long n, int threads) {
+    long long g = (n + threads - 1) / threads;
+    if (g > 152 * 16) g = 152 * 16;
+    return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace
+
+// Workspace layout (each region 256-byte aligned), T = B*L:
+//   f32 [T][max(2P, H)] x2 (A, Bf), bf16 [T][max(2P, H)] x2 (C16, D16),
+//   f32 [2P][H] (dB_bar), f32 [H][2P] (G of dC~), float2 [B][P] (dlambda_bar
+//   partials), f32 [LNB_BLOCKS][H] (dD partials)
+constexpr int LNB_BLOCKS = 304;
+constexpr int LNB_THREADS = 256;
+
+struct StackWs {
+    float *fa, *fb;
+    __nv_bfloat16 *c16, *d16;
+    float *dbbar, *gdc;
+    float2 *dlam;
+    float *ddp;
+};
+static size_t stack_ws_layout(long long T, int B, int H, int P, void *base, StackWs *w) {
+    const long long wdt = (2LL * P > H) ? 2LL * P : (long long)H;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    const size_t o_fa = take(sizeof(float) * T * wdt), o_fb = take(sizeof(float) * T * wdt);
+    const size_t o_c16 = take(2 * T * wdt), o_d16 = take(2 * T * wdt);
+    const size_t o_db = take(sizeof(float) * 2 * P * H), o_g = take(sizeof(float) * 2 * P * H);
+    const size_t o_dl = take(sizeof(float2) * B * P), o_dd = take(sizeof(float) * LNB_BLOCKS * H);
+    if (w && base) {
+        char *c = static_cast<char *>(base);
+        w->fa = reinterpret_cast<float *>(c + o_fa);
+        w->fb = reinterpret_cast<float *>(c + o_fb);
+        w->c16 = reinterpret_cast<__nv_bfloat16 *>(c + o_c16);
+        w->d16 = reinterpret_cast<__nv_bfloat16 *>(c + o_d16);
+        w->dbbar = reinterpret_cast<float *>(c + o_db);
+        w->gdc = reinterpret_cast<float *>(c + o_g);
+        w->dlam = reinterpret_cast<float2 *>(c + o_dl);
+        w->ddp = reinterpret_cast<float *>(c + o_dd);
+    }
+    return off;
+}
+
+}  // namespace s5
+
+// ===========================================================================
+// C entry points (declared in include/s5.h).
+// ===========================================================================
+namespace {
+thread_local char g_err[256] = "";
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+s5_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return S5_OK;
+    std::snprintf(g_err, sizeof(g_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return S5_ERR_CUDA;
+}
+s5_status blas_status(cublasStatus_t s) {
+    if (s == CUBLAS_STATUS_SUCCESS) return S5_OK;
+    std::snprintf(g_err, sizeof(g_err), "cuBLAS status %d", (int)s);
+    return S5_ERR_CUDA;
+}
+#define S5_TRY_CUDA(x) do { s5_status s_ = cuda_status(x); if (s_ != S5_OK) return s_; } while (0)
+#define S5_TRY_BLAS(x) do { s5_status s_ = blas_status(x); if (s_ != S5_OK) return s_; } while (0)
+}  // namespace
+
+extern "C" {
+
+const char *s5_stack_last_error(void) { return g_err; }
+
+size_t s5_stack_workspace_size(int B, int L, int H, int P) {
+    if (B < 1 || L < 1 || H < 1 || P < 1) return 0;
+    return s5::stack_ws_layout((long long)B * L, B, H, P, nullptr, nullptr);
+}
+
+s5_status s5_layernorm(const float *x, float *z, void *z_bf16, long long N, int H, s5_stream_t stream) {
+    if (N < 0 || H < 1 || H > 32 * s5::LN_MAXV) return N < 0 || H < 1 ? S5_ERR_INVALID_ARGUMENT : S5_ERR_UNSUPPORTED;
+    if (N == 0) return S5_OK;
+    if (!x || !z || !al16(x) || !al16(z) || (z_bf16 && !al16(z_bf16))) return S5_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int rows_per_block = 8;
+    s5::ln_fwd_kernel<<<(unsigned)((N + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0, st>>>(
+        x, z, static_cast<__nv_bfloat16 *>(z_bf16), N, H);
+    return cuda_status(cudaGetLastError());
+}
+
+s5_status s5_stack_weights(const float *b_bar, const float *c_tilde, const float *W, int H, int P, void *bs,
+                           void *cp, void *cx, void *w16, s5_stream_t stream) {
+    if (H < 1 || P < 1) return S5_ERR_INVALID_ARGUMENT;
+    const void *ptrs[] = {b_bar, c_tilde, W, bs, cp, cx, w16};
+    for (const void *q : ptrs)
+        if (!q || !al16(q)) return S5_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const long long n = 2LL * P * H + (long long)H * H;
+    s5::stack_weights_kernel<<<s5::grid_for(n, 256), 256, 0, st>>>(
+        reinterpret_cast<const float2 *>(b_bar), reinterpret_cast<const float2 *>(c_tilde), W, H, P,
+        static_cast<__nv_bfloat16 *>(bs), static_cast<__nv_bfloat16 *>(cp), static_cast<__nv_bfloat16 *>(cx),
+        static_cast<__nv_bfloat16 *>(w16));
+    return cuda_status(cudaGetLastError());
+}
+
+s5_status s5_ssm_forward_states(const float *lambda_bar, const void *bs, const void *cp, const float *d,
+                                const float *z, const void *z_bf16, int B, int L, int H, int P,
+                                const float *x0, float *y, float *x, void *X, void *workspace,
+                                size_t workspace_bytes, s5_stream_t stream) {
+    if (B < 1 || L < 1 || H < 1 || P < 1) return S5_ERR_INVALID_ARGUMENT;
+    const void *ptrs[] = {lambda_bar, bs, cp, d, z, z_bf16, y, x, X, workspace};
+    for (const void *q : ptrs)
+        if (!q || !al16(q)) return S5_ERR_INVALID_ARGUMENT;
+    if (x0 && !al16(x0)) return S5_ERR_INVALID_ARGUMENT;
+    const long long T = (long long)B * L;
+    if (T * 2 * P >= (1LL << 31) || T * H >= (1LL << 31)) return S5_ERR_UNSUPPORTED;
+    if (workspace_bytes < s5_stack_workspace_size(B, L, H, P)) return S5_ERR_INVALID_ARGUMENT;
+    s5::StackWs w;
+    s5::stack_ws_layout(T, B, H, P, workspace, &w);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Bu [T][2P] = z16 [T][H] bs^T
+    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)T, 2 * P, H, z_bf16, H, bs, H, w.fa, 2 * P));
+    dim3 grid((P + s5::SCAN_THREADS - 1) / s5::SCAN_THREADS, B);
+    s5::scan_fwd_kernel<<<grid, s5::SCAN_THREADS, 0, st>>>(
+        w.fa, reinterpret_cast<const float2 *>(lambda_bar), reinterpret_cast<const float2 *>(x0), L, P,
+        reinterpret_cast<float2 *>(x), static_cast<__nv_bfloat162 *>(X));
+    S5_TRY_CUDA(cudaGetLastError());
+    // y [T][H] = X [T][2P] cp^T  (the D term is added by the gate's first pass)
+    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)T, H, 2 * P, X, 2 * P, cp, 2 * P, y, H));
+    return S5_OK;
+}
+
+s5_status s5_gate_residual(const float *y_ssm, const float *z, const float *d, const void *w16, const float *u,
+                           long long N, int H, float *y, float *a, float *u_next, void *workspace,
+                           size_t workspace_bytes, s5_stream_t stream) {
+    if (N < 1 || H < 1) return S5_ERR_INVALID_ARGUMENT;
+    const void *ptrs[] = {y_ssm, z, d, w16, u, y, a, u_next, workspace};
+    for (const void *q : ptrs)
+        if (!q || !al16(q)) return S5_ERR_INVALID_ARGUMENT;
+    if (N * H >= (1LL << 31)) return S5_ERR_UNSUPPORTED;
+    if (workspace_bytes < 2 * (size_t)N * H) return S5_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    __nv_bfloat16 *h16 = static_cast<__nv_bfloat16 *>(workspace);
+    const long long n = N * H;
+    s5::gate_pre_kernel<<<s5::grid_for(n, 256), 256, 0, st>>>(y_ssm, z, d, y, h16, n, H);
+    S5_TRY_CUDA(cudaGetLastError());
+    // a [N][H] = h [N][H] W^T
+    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)N, H, H, h16, H, w16, H, a, H));
+    s5::gate_post_kernel<<<s5::grid_for(n, 256), 256, 0, st>>>(u, y, a, u_next, n);
+    return cuda_status(cudaGetLastError());
+}
+
+s5_status s5_gate_backward(const float *ubar, const float *y, const float *a, const void *w16, long long N, int H,
+                           float *ybar, void *ybar_bf16, float *dW, void *workspace, size_t workspace_bytes,
+                           s5_stream_t stream) {
+    if (N < 1 || H < 1) return S5_ERR_INVALID_ARGUMENT;
+    const void *ptrs[] = {ubar, y, a, w16, ybar, ybar_bf16, dW, workspace};
+    for (const void *q : ptrs)
+        if (!q || !al16(q)) return S5_ERR_INVALID_ARGUMENT;
+    if (N * H >= (1LL << 31)) return S5_ERR_UNSUPPORTED;
+    const size_t nh = (size_t)N * H;
+    if (workspace_bytes < nh * (2 + 2 + 4 + 4) + 3 * 256) return S5_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char *c = static_cast<char *>(workspace);
+    __nv_bfloat16 *act16 = reinterpret_cast<__nv_bfloat16 *>(c);
+    __nv_bfloat16 *h16 = reinterpret_cast<__nv_bfloat16 *>(c + s5::align256(2 * nh));
+    float *ydir = reinterpret_cast<float *>(c + 2 * s5::align256(2 * nh));
+    float *wact = reinterpret_cast<float *>(c + 2 * s5::align256(2 * nh) + s5::align256(4 * nh));
+    const long long n = N * H;
+    s5::gate_bwd_pre_kernel<<<s5::grid_for(n, 256), 256, 0, st>>>(ubar, y, a, act16, ydir, h16, n);
+    S5_TRY_CUDA(cudaGetLastError());
+    // W^T act: row-major [N][H] = act [N][H] W [H][H]
+    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)N, H, H, act16, H, w16, H, wact, H));
+    // dW [H][H] = act^T h
+    S5_TRY_BLAS(s5::gemm_rm(st, true, false, H, H, (int)N, act16, H, h16, H, dW, H));
+    s5::gate_bwd_post_kernel<<<s5::grid_for(n, 256), 256, 0, st>>>(ydir, wact, y, ybar,
+                                                                    static_cast<__nv_bfloat16 *>(ybar_bf16), n);
+    return cuda_status(cudaGetLastError());
+}
+
+s5_status s5_ssm_backward(const float *lambda, const float *log_dt, const float *b_tilde, const float *lambda_bar,
+                          const void *bs, const void *cx, const float *d, const float *u, const float *z,
+                          const void *z_bf16, const float *x, const void *X, const float *x0,
+                          const float *ybar, const void *ybar_bf16, const float *ubar_in, int B, int L, int H,
+                          int P, float *ubar_out, float *dlambda, float *dlog_dt, float *db_tilde,
+                          float *dc_tilde, float *dd, void *workspace, size_t workspace_bytes,
+                          s5_stream_t stream) {
+    if (B < 1 || L < 1 || H < 1 || P < 1) return S5_ERR_INVALID_ARGUMENT;
+    if (H > 32 * s5::LN_MAXV) return S5_ERR_UNSUPPORTED;
+    const void *ptrs[] = {lambda, log_dt, b_tilde, lambda_bar, bs, cx, d, u, z, z_bf16, x, X, ybar,
+                          ybar_bf16, ubar_in, ubar_out, dlambda, dlog_dt, db_tilde, dc_tilde, dd, workspace};
+    for (const void *q : ptrs)
+        if (!q || !al16(q)) return S5_ERR_INVALID_ARGUMENT;
+    if (x0 && !al16(x0)) return S5_ERR_INVALID_ARGUMENT;
+    const long long T = (long long)B * L;
+    if (T * 2 * P >= (1LL << 31) || T * H >= (1LL << 31)) return S5_ERR_UNSUPPORTED;
+    if (workspace_bytes < s5_stack_workspace_size(B, L, H, P)) return S5_ERR_INVALID_ARGUMENT;
+    s5::StackWs w;
+    s5::stack_ws_layout(T, B, H, P, workspace, &w);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // x_hat [T][2P] = ybar16 [T][H] cx [H][2P]
+    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)T, 2 * P, H, ybar_bf16, H, cx, 2 * P, w.fa, 2 * P));
+    dim3 grid((P + s5::SCAN_THREADS - 1) / s5::SCAN_THREADS, B);
+    s5::scan_bwd_kernel<<<grid, s5::SCAN_THREADS, 0, st>>>(
+        w.fa, reinterpret_cast<const float2 *>(lambda_bar), reinterpret_cast<const float2 *>(x),
+        reinterpret_cast<const float2 *>(x0), L, P, w.c16, w.dlam);
+    S5_TRY_CUDA(cudaGetLastError());
+    // Re(B_bar^H s) [T][H] = S16 [T][2P] bs [2P][H]
+    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)T, H, 2 * P, w.c16, 2 * P, bs, H, w.fb, H));
+    // dB_bar [2P][H] = S16^T z16
+    S5_TRY_BLAS(s5::gemm_rm(st, true, false, 2 * P, H, (int)T, w.c16, 2 * P, z_bf16, H, w.dbbar, H));
+    // G [H][2P] = ybar16^T X
+    S5_TRY_BLAS(s5::gemm_rm(st, true, false, H, 2 * P, (int)T, ybar_bf16, H, X, 2 * P, w.gdc, 2 * P));
+    // LayerNorm backward (zbar = Re(B_bar^H s) + D ybar) and the residual; dD partials
+    s5::ln_bwd_kernel<<<s5::LNB_BLOCKS, s5::LNB_THREADS, sizeof(float) * (s5::LNB_THREADS / 32) * H, st>>>(
+        u, w.fb, ybar, d, ubar_in, ubar_out, w.ddp, T, H);
+    S5_TRY_CUDA(cudaGetLastError());
+    s5::sum_rows_kernel<<<(H + 255) / 256, 256, 0, st>>>(w.ddp, s5::LNB_BLOCKS, H, dd);
+    S5_TRY_CUDA(cudaGetLastError());
+    s5::zoh_chain_kernel<<<P, 128, 0, st>>>(reinterpret_cast<const float2 *>(lambda), log_dt,
+                                            reinterpret_cast<const float2 *>(b_tilde), w.dbbar, w.dlam, B, H, P,
+                                            reinterpret_cast<float2 *>(dlambda), dlog_dt,
+                                            reinterpret_cast<float2 *>(db_tilde));
+    S5_TRY_CUDA(cudaGetLastError());
+    s5::dc_finish_kernel<<<s5::grid_for((long long)H * P, 256), 256, 0, st>>>(w.gdc, H, P,
+                                                                               reinterpret_cast<float2 *>(dc_tilde));
+    return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

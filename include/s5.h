@@ -145,6 +145,104 @@ s5_status s5_forward_noalloc(const float *lambda_bar, const float *b_bar, const 
                              s5_dtype y_dtype, s5_dtype proj_dtype, int B, int L, int H, int P,
                              const float *x0, float *x_last, s5_stream_t stream);
 
+/* ========================================================================
+ * Layer stack (pre-LayerNorm -> S5 layer -> gated activation -> residual)
+ * and its backward, for general shapes (the deep-stack workload: H = 512,
+ * P = 256, bf16 GEMM operands, complex fp32 scans).  Sources: "SIMPLIFIED
+ * STATE SPACE LAYERS FOR SEQUENCE MODELING" section 6 (pre-norm layers); the
+ * wiki "Method" step 4 and pseudocode (hidden = GELU(y), out = hidden *
+ * sigmoid(W hidden), no bias per its "Paper vs code"); the review's row 4
+ * (residual in the wrapper).  The backward is not on the pages: it is the
+ * chain rule of the forward, with grad(z) = dL/dRe z + i dL/dIm z.
+ *
+ * Shared conventions: device pointers owned by the caller, 16-byte aligned;
+ * T = N = B*L tokens, row-major [T][H] activations; complex arrays are
+ * interleaved (re, im) float pairs.  Dense contractions are bf16 GEMMs with
+ * fp32 accumulation (cuBLAS); every other step runs in this library's
+ * kernels.  Calls are asynchronous on `stream`; the return value reports
+ * argument and launch errors (S5_ERR_CUDA: text in s5_stack_last_error()).
+ * ======================================================================== */
+
+/* Bytes of `workspace` that s5_ssm_forward_states and s5_ssm_backward need;
+ * it also covers s5_gate_residual and s5_gate_backward.  Contents need no
+ * initialisation and are scratch between calls. */
+size_t s5_stack_workspace_size(int B, int L, int H, int P);
+
+/* Text of the last CUDA or cuBLAS error of the stack entry points. */
+const char *s5_stack_last_error(void);
+
+/* LayerNorm over the last axis without affine parameters, biased variance,
+ * eps = 1e-5:  z = (x - mean(x)) / sqrt(var(x) + eps) per row.
+ * x [N][H] f32 -> z [N][H] f32 and, if z_bf16 is not NULL, its bf16 copy.
+ * H <= 1024 (S5_ERR_UNSUPPORTED otherwise).  N = 0 is a no-op. */
+s5_status s5_layernorm(const float *x, float *z, void *z_bf16, long long N, int H,
+                       s5_stream_t stream);
+
+/* bf16 GEMM operands of one layer's weights:
+ *   bs [2P][H]: rows 0..P-1 = Re B_bar, rows P..2P-1 = Im B_bar
+ *   cp [H][2P]: (2 Re C~, -2 Im C~) interleaved per mode (readout, K = 2P)
+ *   cx [H][2P]: [2 Re C~ | -2 Im C~] as two halves (adjoint readout)
+ *   w16 [H][H]: the gate's W
+ * from b_bar [P][H] complex, c_tilde [H][P] complex, W [H][H] f32. */
+s5_status s5_stack_weights(const float *b_bar, const float *c_tilde, const float *W, int H, int P,
+                           void *bs, void *cp, void *cx, void *w16, s5_stream_t stream);
+
+/* S5 layer with its states kept for the backward (review rows 3 and 4; paper
+ * section 3.2 eq. 6, App. H):
+ *   Bu_k = B_bar z_k (bf16 GEMM of z_bf16 and bs),  x_k = lambda_bar x_{k-1} + Bu_k
+ *   (complex fp32, per sequence, from x0 or zero),  y_k = 2 Re(C~ x_k)
+ *   (bf16 GEMM of X and cp).
+ * The feed-through D z_k is NOT included in y: s5_gate_residual adds it.
+ * z [B][L][H] f32 and its bf16 copy -> y [B][L][H] f32, x [B][L][P] complex
+ * f32 (all states), X [B][L][2P] bf16 (states, interleaved Re, Im).
+ * x0 [B][P] complex or NULL.  d is unused here (kept for symmetry). */
+s5_status s5_ssm_forward_states(const float *lambda_bar, const void *bs, const void *cp,
+                                const float *d, const float *z, const void *z_bf16, int B, int L,
+                                int H, int P, const float *x0, float *y, float *x, void *X,
+                                void *workspace, size_t workspace_bytes, s5_stream_t stream);
+
+/* Gated activation and residual (wiki "Method" step 4; review row 4):
+ *   y = y_ssm + d * z,  h = GELU(y) (exact erf form),  a = W h (bf16 GEMM),
+ *   u_next = u + h * sigmoid(a).
+ * y_ssm, z, u [N][H] f32; d [H]; w16 from s5_stack_weights -> y, a, u_next
+ * [N][H] f32 (y and a are kept for the backward).  workspace >= 2*N*H bytes. */
+s5_status s5_gate_residual(const float *y_ssm, const float *z, const float *d, const void *w16,
+                           const float *u, long long N, int H, float *y, float *a, float *u_next,
+                           void *workspace, size_t workspace_bytes, s5_stream_t stream);
+
+/* Backward of the gate: given ubar = dL/du_next [N][H] and the kept y, a:
+ *   act = ubar * h * s (1 - s) with s = sigmoid(a), h = GELU(y),
+ *   ybar = (ubar * s + W^T act) * GELU'(y),  dW = act^T h  (bf16 GEMMs).
+ * -> ybar [N][H] f32 and bf16, dW [H][H] f32.  workspace >= 12*N*H + 768 bytes. */
+s5_status s5_gate_backward(const float *ubar, const float *y, const float *a, const void *w16,
+                           long long N, int H, float *ybar, void *ybar_bf16, float *dW,
+                           void *workspace, size_t workspace_bytes, s5_stream_t stream);
+
+/* Backward of the S5 layer, the LayerNorm and the residual, given ybar =
+ * dL/dy [B][L][H] (f32 and bf16) and ubar_in = dL/du_next:
+ *   x_hat_k = 2 C~^H ybar_k (bf16 GEMM with cx),
+ *   s_k = x_hat_k + conj(lambda_bar) s_{k+1}, s past the end = 0 (reverse scan),
+ *   zbar_k = Re(B_bar^H s_k) + D ybar_k (bf16 GEMM with bs),
+ *   ubar_out = ubar_in + LayerNorm'(u)^T zbar   (u = the layer input),
+ *   dD = sum_k ybar_k z_k,  dC~ = 2 sum_k ybar_k x_k^H,  dB_bar = sum_k s_k z_k^T,
+ *   dlambda_bar = sum_k conj(x_{k-1}) s_k (x_{-1} = x0),
+ * then through the zero-order hold (float64): dB~ = conj(gain) dB_bar,
+ *   dlambda = conj(dt e^z) dlambda_bar + conj(d gain/d lambda) sum_h dB_bar conj(B~),
+ *   dlog_dt = dt (Re(conj(dlambda_bar) lambda e^z) + Re(conj(gphi) e^z)),
+ * gain = (e^z - 1)/lambda, z = lambda dt (series below |z| = 1e-4).
+ * lambda [P], log_dt [P], b_tilde [P][H] are the layer's parameters;
+ * lambda_bar, bs, cx its discretised operands; z, z_bf16, x, X from the
+ * forward.  Outputs: ubar_out [B][L][H] (may alias ubar_in), dlambda [P]
+ * complex, dlog_dt [P], db_tilde [P][H] complex, dc_tilde [H][P] complex,
+ * dd [H].  H <= 1024. */
+s5_status s5_ssm_backward(const float *lambda, const float *log_dt, const float *b_tilde,
+                          const float *lambda_bar, const void *bs, const void *cx, const float *d,
+                          const float *u, const float *z, const void *z_bf16, const float *x,
+                          const void *X, const float *x0, const float *ybar, const void *ybar_bf16,
+                          const float *ubar_in, int B, int L, int H, int P, float *ubar_out,
+                          float *dlambda, float *dlog_dt, float *db_tilde, float *dc_tilde,
+                          float *dd, void *workspace, size_t workspace_bytes, s5_stream_t stream);
+
 /* Waits for `stream`, returns the first device-side condition latched in
  * `workspace` since the last call (S5_OK if none) and clears it. */
 s5_status s5_sync_status(void *workspace, s5_stream_t stream);
