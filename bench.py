@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="pathx_bf16",
-                    choices=["small", "fp32", "pathx_bf16", "irregular"])
+                    choices=["small", "fp32", "pathx_bf16", "irregular", "stack6"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -358,7 +358,9 @@ def run_ours(args):
         "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * 2,
+        # per step: discretize + (weight images + tensor-core forward | CUDA-core forward),
+        # or, with per-step intervals, mode constants + CUDA-core forward
+        "gpu_launches": args.steps * (3 if tc_path else 2),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -370,6 +372,170 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------------------
+STACK_METRIC = "S5 stack training step (fwd+bwd) tokens/s"
+
+
+def stack_flops(B, L, H, P, nl):
+    """Dense flops of one forward + backward step (the bf16 GEMMs): per layer
+    forward Bu (2T*H*2P), readout (2T*2P*H), gate (2T*H*H); backward gate
+    (two of 2T*H*H), x_hat, zbar, dB_bar, dC~ (four of 2T*H*2P)."""
+    T = B * L
+    return nl * (3 * 2 * T * H * 2 * P + 3 * 2 * T * H * H + 4 * 2 * T * H * 2 * P)
+
+
+def run_stack(args):
+    import numpy as np
+    import torch
+
+    from diagonal_state_space_gb300.stack import S5Stack
+    from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = WORKLOADS["stack6"]
+    inp = make_inputs(w)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    u0, G = dev(inp["u0"]), dev(inp["G"])
+    st = S5Stack(inp["params"], w.B, w.L)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st.forward(u0)
+        st.backward(G)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        tt = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = w.B * w.L
+    # end to end: u0 and G from pinned host memory, du0 back
+    u_host = torch.from_numpy(np.ascontiguousarray(inp["u0"])).pin_memory()
+    g_host = torch.from_numpy(np.ascontiguousarray(inp["G"])).pin_memory()
+    du_host = torch.empty(u_host.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        u0.copy_(u_host, non_blocking=True)
+        G.copy_(g_host, non_blocking=True)
+        step()
+        du_host.copy_(st.ubar, non_blocking=True)
+
+    e2e_steps = max(1, min(args.e2e_steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return None
+    _, bf16_tf, peak_kind = load_peaks()
+    flops = stack_flops(w.B, w.L, w.H, w.P, w.layers)
+    achieved = flops / (ms / 1e3) / 1e12
+    result = {
+        "metric": STACK_METRIC, "value": tokens * world / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64 per layer)",
+        "config": {"workload": "stack6: %d layers pre-LN -> S5 -> gate -> residual, forward + "
+                               "backward, B=%d L=%d H=%d P=%d, bf16 GEMM operands, complex fp32 "
+                               "scans" % (w.layers, w.B, w.L, w.H, w.P),
+                   "global_batch": w.B * world, "seq_len": w.L,
+                   "l2": "activations of %.1f GB per step, far above the 129 MB L2"
+                         % (st.u.numel() * 4 * 7 / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "whole step (bf16 GEMMs + scans + elementwise)",
+                     "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_tf if bf16_tf else None,
+                     "peak_source": "%s (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
+                     "flops_per_step": flops, "traffic": None},
+        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * u_host.numel() * 4, "d2h_bytes_per_step": du_host.numel() * 4,
+                "ms_per_step": e2e_ms},
+        # per layer: forward discretize, weights, LayerNorm, scan, gate pre/post; backward
+        # gate pre/post, scan, LayerNorm, dD sum, ZOH chain, dC~ (cuBLAS GEMMs not counted)
+        "gpu_launches": args.steps * w.layers * 13,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = stack_cpu_baseline(w, inp)
+    print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def oracle_stack_run(inp, seqs):
+    import oracle
+    p = dict(inp["params"])
+    p["lambda"] = p.pop("lambda_")
+    return oracle.stack(p, inp["u0"][seqs], inp["G"][seqs])
+
+
+def stack_cpu_baseline(w, inp):
+    """The float64 oracle stack (forward + backward), single-threaded, on one
+    sequence of the workload."""
+    t0 = time.perf_counter()
+    oracle_stack_run(inp, [0])
+    dt = time.perf_counter() - t0
+    return {"value": w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "1 sequence x %d tokens (of %d), %d layers forward + backward, %.1f s"
+                      % (w.L, w.B, w.layers, dt), "host_cores_available": os.cpu_count()}
+
+
+def run_reference_stack(args):
+    from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS["stack6"]
+    inp = make_inputs(w, B=1)
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_stack_run(inp, [0])
+    dt = (time.perf_counter() - t0) / steps
+    v = w.L / dt
+    sample = "1 sequence x %d tokens per step (of %d sequences), %d layers fwd + bwd" % (
+        w.L, w.B, w.layers)
+    res = {"metric": STACK_METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+           "warmup": 0, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P,
+                      "layers": w.layers,
+                      "reference": "float64 CPU oracle (oracle/s5_oracle.c), single thread"},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return res
+
+
 def oracle_run(w, inp, seqs):
     import oracle
     if w.varying_dt:
@@ -395,6 +561,8 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
+    if args.workload == "stack6":
+        return run_reference_stack(args)
     from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
     w = WORKLOADS[args.workload]
     inp = make_inputs(w)
@@ -426,6 +594,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack6":
+        run_stack(args)
     else:
         run_ours(args)
 
