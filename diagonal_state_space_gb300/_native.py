@@ -8,7 +8,7 @@ import threading
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libs5.so")
 
 S5_F32, S5_BF16 = 0, 1
-S5_NOALLOC_SCRATCH_BYTES = 8 << 20   # include/s5.h
+S5_NOALLOC_SCRATCH_BYTES = 16 << 20   # include/s5.h
 STATUS = {0: "S5_OK", 1: "S5_ERR_INVALID_ARGUMENT", 2: "S5_ERR_UNSUPPORTED", 3: "S5_ERR_CUDA",
           4: "S5_ERR_TIMEOUT", 5: "S5_ERR_NONFINITE"}
 

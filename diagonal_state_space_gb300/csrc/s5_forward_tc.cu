@@ -6,15 +6,15 @@
 //
 // Work split.  A sequence of nchunks tiles (64 tokens each) is spread over W
 // "lanes" (CTAs): lane p of sequence b takes chunks p, p+W, p+2W, ...  With
-// Lam = lambda_bar^64 and E(q) the end state of chunk q from a zero start, the
-// state entering chunk c of a lane follows from its own previous chunk c-W:
-//   S(c) = Lam^(W-1) x_end(c-W) + sum_{q=c-W+1}^{c-1} Lam^(c-1-q) E(q),
-// and for the lane's first chunk (c < W): S(c) = Lam^c x0 + sum_{q<c} Lam^(c-1-q) E(q).
-// Every E(q) is known once chunk q's own scan (pass 1) has run, so no tile
-// waits for another tile's final state: there is no carry chain across CTAs,
-// only W-1 aggregate records to read per tile.  Grid: B*W CTAs (one per SM,
-// cooperative launch so that all are resident); when B exceeds the SM count,
-// W = 1 and each CTA takes whole sequences.
+// Lam = lambda_bar^64 and E(q) the end state of chunk q from a zero start
+// (published by q's lane after its first scan pass), the state entering chunk
+// q+1 is S(q+1) = Lam S(q) + E(q).  One more CTA per sequence, the sequence's
+// scanner, runs exactly that chunk-level recurrence (in registers, one thread
+// per mode): it reads each E(q) once and publishes every S(q).  Each lane then
+// reads one record per tile: its carry.  Grid: B*(W+1) CTAs (one per SM,
+// cooperative launch so that all are resident); when fewer than three CTAs per
+// sequence fit, W = 1 and each CTA takes whole sequences with the carry passed
+// on in registers.
 //
 // Each CTA runs a warp-specialised pipeline over its tiles:
 //   warps 0-3   TMA and tcgen05.mma issue (one thread each):
@@ -33,9 +33,9 @@
 //               operand X [64 x 2P]
 //   warps 8-11  epilogue, thread = feature = TMEM lane of GEMM2:
 //               y = D2 + D*u (u re-read through L2), bf16 stores
-//   warps 12-15 carry windows, thread = mode: fold the aggregate records that
-//               each tile's carry needs into a shared-memory slot (two slots),
-//               running ahead of the scan.
+//   warps 12-15 carries, thread = mode: wait for the tile's carry record and
+//               put it into a shared-memory slot (two slots), ahead of the scan.
+// The scanner CTAs run none of this: threads 0..P-1 only.
 // Bs holds B_bar split into real rows (0..P-1) and imaginary rows (P..2P-1);
 // C' interleaves (2 Re C~, -2 Im C~) so that K = 2P of GEMM2 pairs with X's
 // interleaved (Re x, Im x): sum_k C'[h][k] X[t][k] = 2 Re(C~ x_t)[h].
@@ -192,12 +192,14 @@ __device__ __forceinline__ void st_record(float4 *p, float2 e, unsigned tag) {
                  : "memory");
 }
 
-// Lane geometry: CTA k of G.  W > 1: one lane (b = k % B, p = k / B) with
-// chunks p, p + W, ...  W == 1: sequences k, k + G, ..., every chunk.
+// Lane geometry: CTA k of G.  W > 1: CTAs k < B*W are lanes (b = k % B,
+// p = k / B) with chunks p, p + W, ...; CTAs k >= B*W are the scanners of
+// sequences k - B*W.  W == 1: sequences k, k + G, ..., every chunk.
 struct Lane {
     int B, W, G, k, nchunks;
+    __device__ __forceinline__ bool scanner() const { return W > 1 && k >= B * W; }
     __device__ __forceinline__ int count() const {
-        if (W > 1) return (nchunks - k / B + W - 1) / W;
+        if (W > 1) return scanner() ? 0 : (nchunks - k / B + W - 1) / W;
         return (k < B ? (B - k + G - 1) / G : 0) * nchunks;
     }
     __device__ __forceinline__ void tile(int i, int &b, int &c) const {
@@ -211,72 +213,77 @@ struct Lane {
     }
 };
 
-// Folds the aggregate records that the carry of chunk c (sequence b) needs
-// for mode m: sum_q Lam^(c-1-q) E(q) over the window q in [c-W+1, c) (or
-// [0, c) when c < W), Horner from the oldest record.  The newest record of the
-// window (the last one to be published, as lanes advance together) is polled
-// alone, with backoff, before the window is read; records still missing then
-// are re-read.  A wait that runs out latches S5_ERR_TIMEOUT and folds zeros in
-// place of the missing records, so that the launch still completes.
-__device__ float2 fold_window(const float4 *rec, int b, int c, int nchunks, int W, int m, float2 Lam,
-                              unsigned tag, WsHeader *hdr, unsigned long long limit, bool &gave_up) {
-    const int lo = c < W ? 0 : c - W + 1;
-    const int n = c < W ? c : W - 1;
-    float2 acc = make_float2(0.f, 0.f);
-    if (n == 0) return acc;
-    const size_t seq = (size_t)b * nchunks;
-    unsigned long long t0 = 0;
-    unsigned backoff = 64;
-    bool timing = false;
-    // wait for the newest record
-    while (!gave_up && __float_as_uint(ld_record(rec + (seq + c - 1) * P_M + m).w) != tag) {
-        if (!timing) {
-            t0 = global_ns();
-            timing = true;
-        } else if (global_ns() - t0 > limit) {
+// Waits (bounded) until the 16-byte record at p carries `tag`; returns its
+// value.  A wait that runs out latches S5_ERR_TIMEOUT (once per thread) and
+// returns zero, so that the launch still completes.
+__device__ float2 wait_record(const float4 *p, unsigned tag, WsHeader *hdr, unsigned long long limit,
+                              bool &gave_up, unsigned tile) {
+    float4 v = ld_record(p);
+    if (__float_as_uint(v.w) == tag) return make_float2(v.x, v.y);
+    const unsigned long long t0 = global_ns();
+    while (!gave_up) {
+        __nanosleep(64);
+        v = ld_record(p);
+        if (__float_as_uint(v.w) == tag) return make_float2(v.x, v.y);
+        if (global_ns() - t0 > limit) {
             latch_status(hdr, S5_ERR_TIMEOUT);
-            atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + c) + 1u);
+            atomicCAS(&hdr->timeout_tile, 0u, tile + 1u);
             gave_up = true;
-            break;
         }
-        __nanosleep(backoff);
-        if (backoff < 1024) backoff <<= 1;
     }
-    for (int base = 0; base < n; base += RB) {
-        const int nr = min(RB, n - base);
-        const float4 *rp = rec + (seq + lo + base) * P_M + m;
+    return make_float2(0.f, 0.f);
+}
+
+// The sequence scanner (thread = mode m): S(0) = x0, then for every chunk q
+// in order, publish S(q) (tag_s) and advance S(q+1) = Lam S(q) + E(q).  The
+// aggregates E(q) (tag_e) of a group of R consecutive chunks are loaded in one
+// round; the published prefix is folded and its S values go out at once, and
+// the rest of the group is re-read in one round (bounded) until complete.
+// R <= W: a group then spans at most two waves, and a lane's aggregate of
+// wave g needs only its carry of wave g-2, so no group waits on its own
+// carries.
+__device__ __noinline__ void scanner_loop(const float4 *agg, float4 *carry, size_t seq, int nchunks, int R,
+                                          float2 S, float2 Lam, unsigned tag_e, unsigned tag_s, WsHeader *hdr,
+                                          unsigned long long limit) {
+    bool gave_up = false;
+    for (int q0 = 0; q0 < nchunks; q0 += R) {
+        const int nr = min(R, nchunks - q0);
+        const float4 *rp = agg + (seq + q0) * P_M;
+        st_record(carry + (seq + q0) * P_M, S, tag_s);
         float4 v[RB];
+        int done = 0;   // records of the group folded so far
+        unsigned long long t0 = 0;
+        bool timing = false;
         for (;;) {
-            bool ready = true;
+#pragma unroll
+            for (int w = 0; w < RB; ++w)
+                if (w >= done && w < nr) v[w] = ld_record(rp + (size_t)w * P_M);
+            bool prefix = true;
 #pragma unroll
             for (int w = 0; w < RB; ++w) {
-                v[w] = (w < nr) ? ld_record(rp + (size_t)w * P_M) : make_float4(0.f, 0.f, 0.f, 0.f);
-                if (w < nr && __float_as_uint(v[w].w) != tag) ready = false;
+                if (w >= done && w < nr && prefix) {
+                    if (__float_as_uint(v[w].w) == tag_e || gave_up) {
+                        const bool ok = __float_as_uint(v[w].w) == tag_e;
+                        S = cfma(Lam, S, ok ? make_float2(v[w].x, v[w].y) : make_float2(0.f, 0.f));
+                        if (w + 1 < nr) st_record(carry + (seq + q0 + w + 1) * P_M, S, tag_s);
+                        done = w + 1;
+                    } else {
+                        prefix = false;
+                    }
+                }
             }
-            if (ready) break;
-            if (gave_up) {
-#pragma unroll
-                for (int w = 0; w < RB; ++w)
-                    if (__float_as_uint(v[w].w) != tag) v[w] = make_float4(0.f, 0.f, 0.f, 0.f);
-                break;
-            }
+            if (done >= nr) break;
             if (!timing) {
                 t0 = global_ns();
                 timing = true;
             } else if (global_ns() - t0 > limit) {
                 latch_status(hdr, S5_ERR_TIMEOUT);
-                atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + c) + 1u);
+                atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + q0 + done) + 1u);
                 gave_up = true;
-                continue;   // one more pass zeroes what is missing
             }
-            __nanosleep(backoff);
-            if (backoff < 1024) backoff <<= 1;
+            __nanosleep(32);
         }
-#pragma unroll
-        for (int w = 0; w < RB; ++w)
-            if (w < nr) acc = cfma(Lam, acc, make_float2(v[w].x, v[w].y));
     }
-    return acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -444,10 +451,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     ln.k = (int)blockIdx.x;
     ln.nchunks = nchunks;
     const int n = ln.count();
+    const bool scanner = ln.scanner();
     // the allocation must hold the 1024-aligned layout (the same for every thread)
     const bool fits = pad + SM_TOTAL <= SMEM_REQUEST;
 
-    if (fits) {
+    if (fits && scanner) {
+        // ------------------------------------------------------------ sequence scanner
+        if (threadIdx.x < P_M) {
+            const int m = threadIdx.x, b = ln.k - B * W;
+            const unsigned ep = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
+            const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
+            const float2 S0 = args.x0 ? args.x0[(size_t)b * P_M + m] : make_float2(0.f, 0.f);
+            scanner_loop(args.ws.agg + m, args.ws.carry + m, (size_t)b * nchunks, nchunks, min(RB, W), S0,
+                         cpow(args.lambda_bar[m], 64), (ep << 2) | FLAG_AGG, (ep << 2) | FLAG_INCL, hdr,
+                         1000ull * (lim ? lim : 1000000u));
+        }
+    } else if (fits) {
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&sb->full_u[s], 1);
@@ -483,10 +502,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = fits ? sb->tmem_base : 0u;
-    const unsigned tag = fits ? ((sb->epoch << 2) | FLAG_AGG) : 0u;
+    const bool pipeline = fits && !scanner;
+    const uint32_t tmem = pipeline ? sb->tmem_base : 0u;
+    const unsigned tag = pipeline ? ((sb->epoch << 2) | FLAG_AGG) : 0u;
 
-    if (!fits) {
+    if (!pipeline) {
         // nothing to run: straight to the teardown
     } else if (warp < 4) {
         // ------------------------------------------------------------ TMA + MMA issue
@@ -594,7 +614,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         kc.lb = args.lambda_bar[m];
         kc.lb32 = cpow(kc.lb, 32);
         kc.lb64 = cmul(kc.lb32, kc.lb32);
-        const float2 lw1 = cpow(kc.lb64, W - 1);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const uint32_t xcol = (uint32_t)lane * 4u;   // byte of (Re, Im) in this warp's k-block row
         // shared address of (row q, this lane's column) in each swizzle phase q;
@@ -626,19 +645,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             if (mine && front)
                 mine = scan_front(t2, i + 2, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
             if (!named_bar_and(BAR_SCAN, 128, mine)) break;
-            // carry of tile i: window sum from the fold warps' slot
-            mine = pipe_wait(&sb->carry_full[i & 1], (i >> 1) & 1, sb, hdr);
-            if (mine) {
-                const float2 wsum = slots[(i & 1) * P_M + m];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sb->carry_empty[i & 1]);
-                float2 carry;
-                if (t0.c < W) {
-                    const float2 x0v = args.x0 ? args.x0[(size_t)t0.b * P_M + m] : make_float2(0.f, 0.f);
-                    carry = cfma(cpow(kc.lb64, t0.c), x0v, wsum);
-                } else {
-                    carry = cfma(lw1, xprev, wsum);
+            // carry of tile i: from the carry warps' slot, or (one lane per
+            // sequence) the previous tile's end state
+            float2 carry = xprev;
+            if (W > 1) {
+                mine = pipe_wait(&sb->carry_full[i & 1], (i >> 1) & 1, sb, hdr);
+                if (mine) {
+                    carry = slots[(i & 1) * P_M + m];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sb->carry_empty[i & 1]);
                 }
+            } else if (t0.c == 0) {
+                carry = args.x0 ? args.x0[(size_t)t0.b * P_M + m] : make_float2(0.f, 0.f);
+            }
+            if (mine) {
                 // pass 2 of tile i once GEMM2 of tile i-1 has read X
                 mine = i == 0 || pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr);
                 if (mine) {
@@ -694,33 +714,29 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sb->tmem_empty[r]);
                 }
-                if (Tc == T_TOK) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        yrow[(size_t)(ch * 16 + k) * H_F] = __float2bfloat16_rn(
-                            fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (ch * 16 + k < Tc)
-                            yrow[(size_t)(ch * 16 + k) * H_F] = __float2bfloat16_rn(
-                                fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
-                }
+                for (int k = 0; k < 16; ++k)
+                    if (ch * 16 + k < Tc)
+                        yrow[(size_t)(ch * 16 + k) * H_F] =
+                            __float2bfloat16_rn(fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
             }
         }
-    } else if (warp >= W_FOLD && warp < W_FOLD + 4) {
-        // ------------------------------------------------------------ carry windows
+    } else if (warp >= W_FOLD && warp < W_FOLD + 4 && W > 1) {
+        // ------------------------------------------------------------ carries
         const int m = 32 * (warp - W_FOLD) + lane;
-        const float2 lam = cpow(args.lambda_bar[m], 64);
         float2 *slots = reinterpret_cast<float2 *>(smem + SM_CARRY);
+        const float4 *carry = args.ws.carry;
+        const unsigned tag_s = (sb->epoch << 2) | FLAG_INCL;
         const unsigned long long limit = sb->limit_ns;
+        const int b = ln.k % B, p = ln.k / B;
+        const size_t seq = (size_t)b * nchunks;
         bool gave_up = false;
         for (int j = 0; j < n; ++j) {
-            // slot j % 2 is free once the scan has read tile j-2's sum
+            // slot j % 2 is free once the scan has read tile j-2's carry
             if (j >= 2 && !pipe_wait(&sb->carry_empty[j & 1], ((j >> 1) - 1) & 1, sb, hdr)) break;
-            int b, c;
-            ln.tile(j, b, c);
-            slots[(j & 1) * P_M + m] = fold_window(rec, b, c, nchunks, W, m, lam, tag, hdr, limit, gave_up);
+            const float2 own = wait_record(carry + (seq + (size_t)j * W + p) * P_M + m, tag_s, hdr, limit,
+                                           gave_up, (unsigned)(seq + (size_t)j * W + p));
+            slots[(j & 1) * P_M + m] = own;
             __syncwarp();
             if (lane == 0) mbar_arrive(&sb->carry_full[j & 1]);
         }
@@ -730,7 +746,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (fits && warp == W_TMEM) tmem_dealloc(tmem, 512);
+    if (pipeline && warp == W_TMEM) tmem_dealloc(tmem, 512);
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&hdr->done_counter, 1u);
@@ -778,18 +794,19 @@ bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16) {
     return H == H_F && P == P_M && u_bf16 && y_bf16 && proj_bf16;
 }
 
-// Lanes per sequence and grid: B * W CTAs (W <= nchunks, W <= W_MAX) when the
-// sequences fit on the SMs, else W = 1 and one CTA per SM.
+// Lanes per sequence and grid: W lanes plus one scanner per sequence, B*(W+1)
+// CTAs (2 <= W <= nchunks, W <= W_MAX), when at least three CTAs per sequence
+// fit on the SMs; else W = 1, min(B, SMs) CTAs, each taking whole sequences.
 void tc_grid(int B, int nchunks, int num_sms, int *W, int *G) {
-    if (B <= num_sms) {
-        int w = num_sms / B;
-        if (w > nchunks) w = nchunks;
-        if (w > W_MAX) w = W_MAX;
+    int w = B <= num_sms ? num_sms / B - 1 : 0;
+    if (w > nchunks) w = nchunks;
+    if (w > W_MAX) w = W_MAX;
+    if (w >= 2) {
         *W = w;
-        *G = B * w;
+        *G = B * (w + 1);
     } else {
         *W = 1;
-        *G = num_sms;
+        *G = B < num_sms ? B : num_sms;
     }
 }
 

@@ -16,7 +16,9 @@ namespace s5 {
 // zero start) and then its inclusive end state.  Layout (each region 256-byte
 // aligned):
 //   header (256 B) | flags [ntiles] u32 | agg [ntiles][P] float4 |
-//   incl [ntiles][P] float2 | mode constants [P] ModeConst |
+//   incl [ntiles][P] 16 bytes (the CUDA-core path uses the first 8 bytes of
+//   each, as float2; the tensor-core path whole, as carry records) |
+//   mode constants [P] ModeConst |
 //   operand images [8*P*H bytes] (bf16 weights of the tensor-core path)
 // Flags carry a launch epoch in their upper 30 bits so that a workspace needs
 // no clearing between calls: the last CTA of every launch bumps the epoch and
@@ -53,7 +55,8 @@ struct WsLayout {
     WsHeader *hdr;
     unsigned int *flags;
     float4 *agg;
-    float2 *incl;
+    float2 *incl;     // [ntiles][P] float2 (CUDA-core path)
+    float4 *carry;    // the same region as [ntiles][P] float4 (tensor-core path)
     ModeConst *modes;
     unsigned char *wimg;
 };
@@ -66,7 +69,7 @@ __host__ __device__ inline size_t ws_bytes(long long ntiles, int P, int H) {
     size_t s = 256;
     s += align256(sizeof(unsigned int) * (size_t)ntiles);
     s += align256(sizeof(float4) * (size_t)ntiles * P);
-    s += align256(sizeof(float2) * (size_t)ntiles * P);
+    s += align256(sizeof(float4) * (size_t)ntiles * P);
     s += align256(sizeof(ModeConst) * (size_t)P);
     s += 1024 + wimg_bytes(P, H);   // images start 1024-byte aligned
     return s;
@@ -82,7 +85,8 @@ inline WsLayout ws_layout(void *base, long long ntiles, int P) {
     w.agg = reinterpret_cast<float4 *>(p);
     p += align256(sizeof(float4) * (size_t)ntiles * P);
     w.incl = reinterpret_cast<float2 *>(p);
-    p += align256(sizeof(float2) * (size_t)ntiles * P);
+    w.carry = reinterpret_cast<float4 *>(p);
+    p += align256(sizeof(float4) * (size_t)ntiles * P);
     w.modes = reinterpret_cast<ModeConst *>(p);
     p += align256(sizeof(ModeConst) * (size_t)P);
     // 1024-byte alignment keeps the swizzle pattern of the images intact

@@ -139,7 +139,7 @@ size_t s5_workspace_size(int B, int L, int H, int P);
  *    streams, other host threads) race and give wrong results.  Serialize them.
  *  - Device-side conditions (a carry wait that gave up) are not reported.
  */
-#define S5_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define S5_NOALLOC_SCRATCH_BYTES (16u << 20)
 s5_status s5_forward_noalloc(const float *lambda_bar, const float *b_bar, const float *c_tilde,
                              const float *d, const void *u, s5_dtype u_dtype, void *y,
                              s5_dtype y_dtype, s5_dtype proj_dtype, int B, int L, int H, int P,
