@@ -33,7 +33,7 @@ def _host(t):
     return t.detach().cpu().numpy()
 
 
-@pytest.mark.parametrize("N,H", [(1, 1), (333, 200), (64, 512), (17, 1024)])
+@pytest.mark.parametrize("N,H", [(1, 1), (9, 100), (333, 200), (64, 512), (7, 130), (17, 1024)])
 def test_layernorm_matches_oracle(N, H):
     rng = np.random.default_rng(N + H)
     x = (rng.standard_normal((N, H)) * 3 + 1.5).astype(np.float32)
@@ -45,7 +45,7 @@ def test_layernorm_matches_oracle(N, H):
 
 
 @pytest.mark.parametrize("B,L,H,P,nl", [(1, 1, 32, 16, 1), (2, 77, 64, 32, 2), (3, 130, 48, 40, 2),
-                                        (2, 257, 128, 64, 3)])
+                                        (2, 257, 128, 64, 3), (2, 66, 30, 20, 1), (1, 200, 256, 96, 2)])
 def test_stack_forward_backward_matches_oracle(B, L, H, P, nl):
     inp = make_stack_inputs(B, L, H, P, nl, seed=97 * B + L)
     st = s5stack.S5Stack(inp["params"], B, L)
