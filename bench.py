@@ -479,9 +479,10 @@ def run_stack(args):
         "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * u_host.numel() * 4, "d2h_bytes_per_step": du_host.numel() * 4,
                 "ms_per_step": e2e_ms},
-        # per layer: forward discretize, weights, LayerNorm, scan, gate pre/post; backward
-        # gate pre/post, scan, LayerNorm, dD sum, ZOH chain, dC~ (cuBLAS GEMMs not counted)
-        "gpu_launches": args.steps * w.layers * 13,
+        # per step one discretize of all layers' modes; per layer: forward weights,
+        # LayerNorm, scan aggregates + apply, gate pre/post; backward gate pre/post,
+        # scan aggregates + apply, LayerNorm, dD sum, ZOH chain, dC~ (cuBLAS GEMMs not counted)
+        "gpu_launches": args.steps * (1 + w.layers * 14),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

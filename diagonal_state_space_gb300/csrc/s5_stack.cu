@@ -312,13 +312,24 @@ __global__ void ln_bwd_vec_kernel(const float *__restrict__ x, const float *__re
     }
 }
 
-// out[h] = sum_b part[b][h]  (fixed order: deterministic)
+// out[h] = sum_b part[b][h] in a fixed order (deterministic): block
+// (32 columns) x (SUM_GROUPS row groups), each group summing rows
+// g, g + SUM_GROUPS, ..., then the groups in order.
+constexpr int SUM_GROUPS = 32;
 __global__ void sum_rows_kernel(const float *__restrict__ part, int nb, int H, float *__restrict__ out) {
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= H) return;
+    __shared__ float s_part[SUM_GROUPS][33];
+    const int h = blockIdx.x * 32 + threadIdx.x, g = threadIdx.y;
     float t = 0.f;
-    for (int b = 0; b < nb; ++b) t += part[(size_t)b * H + h];
-    out[h] = t;
+    if (h < H)
+#pragma unroll 4
+        for (int b = g; b < nb; b += SUM_GROUPS) t += part[(size_t)b * H + h];
+    s_part[g][threadIdx.x] = t;
+    __syncthreads();
+    if (g == 0 && h < H) {
+        float r = 0.f;
+        for (int q = 0; q < SUM_GROUPS; ++q) r += s_part[q][threadIdx.x];
+        out[h] = r;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -611,16 +622,20 @@ __global__ void zoh_chain_kernel(const float2 *__restrict__ lambda, const float 
                                  float2 *__restrict__ db_tilde) {
     const int p = blockIdx.x;
     __shared__ dc s_gain, s_red[32], s_redl[32];
-    __shared__ dc s_gphi;
+    __shared__ double s_tr[5];   // sin z.im, cos z.im, exp z.re, expm1 z.re, sin(z.im / 2)
     const float2 l = lambda[p];
     const dc lam = {(double)l.x, (double)l.y};
     const double dt = exp((double)log_dt[p]);
     const dc z = {lam.re * dt, lam.im * dt};
+    // the four fp64 transcendentals side by side, one thread each
+    if (threadIdx.x == 0) sincos(z.im, &s_tr[0], &s_tr[1]);
+    else if (threadIdx.x == 1) s_tr[2] = exp(z.re);
+    else if (threadIdx.x == 2) s_tr[3] = expm1(z.re);
+    else if (threadIdx.x == 3) s_tr[4] = sin(0.5 * z.im);
+    __syncthreads();
     if (threadIdx.x == 0) {
         const double zabs = sqrt(z.re * z.re + z.im * z.im);
-        double sn, cs;
-        sincos(z.im, &sn, &cs);
-        const double mag = exp(z.re);
+        const double sn = s_tr[0], cs = s_tr[1], mag = s_tr[2];
         if (zabs < 1e-4) {
             dc term = {1.0, 0.0}, phi = {1.0, 0.0};
             for (int n = 1; n <= 8; ++n) {
@@ -632,8 +647,8 @@ __global__ void zoh_chain_kernel(const float2 *__restrict__ lambda, const float 
             }
             s_gain = {dt * phi.re, dt * phi.im};
         } else {
-            const double sh = sin(0.5 * z.im);
-            const dc em1 = {expm1(z.re) * cs - 2.0 * sh * sh, mag * sn};
+            const double sh = s_tr[4];
+            const dc em1 = {s_tr[3] * cs - 2.0 * sh * sh, mag * sn};
             s_gain = dc_div(em1, lam);
         }
     }
@@ -674,15 +689,12 @@ __global__ void zoh_chain_kernel(const float2 *__restrict__ lambda, const float 
             gp.re += s_red[w].re;
             gp.im += s_red[w].im;
         }
-        s_gphi = gp;
         dc gl = {0.0, 0.0};
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
             gl.re += s_redl[w].re;
             gl.im += s_redl[w].im;
         }
-        double sn, cs;
-        sincos(z.im, &sn, &cs);
-        const double mag = exp(z.re);
+        const double sn = s_tr[0], cs = s_tr[1], mag = s_tr[2];
         const dc ab = {mag * cs, mag * sn};
         const double zabs = sqrt(z.re * z.re + z.im * z.im);
         dc dg;
@@ -991,7 +1003,7 @@ s5_status s5_ssm_backward(const float *lambda, const float *log_dt, const float 
         s5::ln_bwd_kernel<<<s5::LNB_BLOCKS, s5::LNB_THREADS, ln_smem, st>>>(u, w.fb, ybar, d, ubar_in, ubar_out,
                                                                           w.ddp, T, H);
     S5_TRY_CUDA(cudaGetLastError());
-    s5::sum_rows_kernel<<<(H + 255) / 256, 256, 0, st>>>(w.ddp, s5::LNB_BLOCKS, H, dd);
+    s5::sum_rows_kernel<<<(H + 31) / 32, dim3(32, s5::SUM_GROUPS), 0, st>>>(w.ddp, s5::LNB_BLOCKS, H, dd);
     S5_TRY_CUDA(cudaGetLastError());
     s5::zoh_chain_kernel<<<P, 128, 0, st>>>(reinterpret_cast<const float2 *>(lambda), log_dt,
                                             reinterpret_cast<const float2 *>(b_tilde), w.dbbar, w.dlam, B * NC, H, P,

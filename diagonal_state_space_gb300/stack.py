@@ -86,10 +86,11 @@ class S5Stack:
         lib, st = _native.lib(), _stream()
         B, L, H, P, T = self.B, self.L, self.H, self.P, self.T
         self.u[0].copy_(torch.as_tensor(u0, dtype=_F32).reshape(B, L, H))
+        # the zero-order hold acts per mode: all layers' modes in one call
+        check("s5_discretize", lib.s5_discretize(
+            _p(self.lam), _p(self.log_dt), _p(self.b_tilde), self.nl * P, H, _p(self.lbar),
+            _p(self.bbar), st))
         for l in range(self.nl):
-            check("s5_discretize", lib.s5_discretize(
-                _p(self.lam[l]), _p(self.log_dt[l]), _p(self.b_tilde[l]), P, H, _p(self.lbar[l]),
-                _p(self.bbar[l]), st))
             check("s5_stack_weights", lib.s5_stack_weights(
                 _p(self.bbar[l]), _p(self.c_tilde[l]), _p(self.W[l]), H, P, _p(self.bs[l]),
                 _p(self.cp[l]), _p(self.cx[l]), _p(self.w16[l]), st))
