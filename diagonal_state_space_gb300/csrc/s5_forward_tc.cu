@@ -58,10 +58,10 @@ namespace {
 constexpr int T_TOK = TC_TILE_TOKENS;   // tokens per tile (N of both GEMMs)
 constexpr int H_F = 128;                // features
 constexpr int P_M = 128;                // stored complex modes
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int REGIONS = 4;              // TMEM regions of 128 columns
 constexpr int THREADS = 512;
-constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;
+constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;   // warp 3 is idle
 constexpr int W_MAX = 64;               // lanes per sequence at most
 constexpr int RB = 18;                  // aggregate records loaded per round
 constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps
@@ -72,10 +72,11 @@ constexpr uint32_t SM_BS = 0;
 constexpr uint32_t SM_CP = SM_BS + BS_BYTES;
 constexpr uint32_t SM_U = SM_CP + CP_BYTES;            // [stage][2 kb][64 rows][128 B]
 constexpr uint32_t U_STAGE = 2 * T_TOK * 128;
-constexpr uint32_t SM_X = SM_U + STAGES * U_STAGE;     // [4 kb][64 rows][128 B]
+constexpr uint32_t SM_EU = SM_U + STAGES * U_STAGE;    // the epilogue's copy of u: [2 kb][64 rows][128 B]
+constexpr uint32_t SM_X = SM_EU + U_STAGE;             // [4 kb][64 rows][128 B]
 constexpr uint32_t SM_CARRY = SM_X + 4 * T_TOK * 128;  // [2 slots][P] float2
 constexpr uint32_t SM_BAR = SM_CARRY + 2 * P_M * 8;
-constexpr uint32_t SM_TOTAL = SM_BAR + 256;
+constexpr uint32_t SM_TOTAL = SM_BAR + 512;
 // Dynamic shared memory is requested up to the per-block limit; the slack
 // absorbs the rounding of its base up to 1024 bytes (checked at run time).
 constexpr uint32_t SMEM_REQUEST = 227 * 1024;
@@ -87,15 +88,17 @@ constexpr unsigned long long DRAIN_WAIT_NS = 200000000ull;   // 0.2 s per teardo
 
 struct Bars {
     uint64_t full_u[STAGES], empty_u[STAGES];
-    uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], mma2_done[REGIONS];
-    uint64_t xready, xfree, weights, drain;
+    uint64_t eu_full, eu_empty;     // the epilogue's u buffer
+    uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], p2read[REGIONS], mma2_done[REGIONS];
+    uint64_t xready, xfree;         // X written by the four scan warps / read by GEMM2
+    uint64_t weights, drain;
     uint64_t carry_full[2], carry_empty[2];
     unsigned long long limit_ns;   // aggregate-record wait limit
     uint32_t tmem_base;
     unsigned epoch, drop;
     int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 __device__ __forceinline__ bool aborted(Bars *sb) {
     return *reinterpret_cast<volatile int *>(&sb->abort) != 0;
@@ -110,8 +113,7 @@ __device__ __forceinline__ void set_abort(Bars *sb, WsHeader *hdr) {
 // completes, so it takes no issue slots from the warps sharing its SM
 // sub-partition.
 constexpr uint32_t SLEEP_HINT_NS = 1000000;   // re-check abort/limits every 1 ms
-__device__ __forceinline__ bool pipe_wait(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool pipe_wait_slow(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
@@ -121,6 +123,9 @@ __device__ __forceinline__ bool pipe_wait(uint64_t *bar, uint32_t parity, Bars *
             return false;
         }
     }
+}
+__device__ __forceinline__ bool pipe_wait(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
+    return mbar_try_wait(bar, parity) || pipe_wait_slow(bar, parity, sb, hdr);
 }
 // Teardown wait: bounded, ignores the abort flag.
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -287,37 +292,45 @@ __device__ __noinline__ void scanner_loop(const float4 *agg, float4 *carry, size
 }
 
 // ---------------------------------------------------------------------------
-// Scan passes over one tile of this thread's mode (TMEM lane): D1 columns
-// [col0, col0+64) hold Re(Bu_t), [col0+64, col0+128) hold Im(Bu_t).
+// Scan passes over one tile of this thread's mode (TMEM lane): columns
+// [col0, col0+64) hold Re(Bu_t), [col0+64, col0+128) hold Im(Bu_t).  A full
+// tile runs as four independent 16-token chains (tokens 16q .. 16q+15), so
+// that the FMA pipe, not the chain's latency, sets the pace.
 // ---------------------------------------------------------------------------
 struct ScanConsts {
-    float2 lb, lb32, lb64;   // lambda_bar and its powers
+    float2 lb, lb16;   // lambda_bar, lambda_bar^16
 };
 
-// Full tile: end state from zero over tokens 0..31 (elo) and 0..63 (returned),
-// as two interleaved 32-step chains over tokens 0..31 and 32..63.
-__device__ __forceinline__ float2 pass1_full(uint32_t col0, const ScanConsts &k, float2 &elo) {
-    float2 ea = make_float2(0.f, 0.f), ez = make_float2(0.f, 0.f);
+// Full tile, pass 1: the four chains' end states from zero (e[0..2] kept for
+// pass 2); returns the tile's end state from zero, (((e0 L + e1) L + e2) L + e3)
+// with L = lambda_bar^16.
+__device__ __forceinline__ float2 pass1_full(uint32_t col0, const ScanConsts &k, float2 (&e)[3]) {
+    float2 c0 = make_float2(0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
 #pragma unroll 1
-    for (int c8 = 0; c8 < 4; ++c8) {
-        uint32_t ra[8], ia[8], rz[8], iz[8];
-        tmem_ld8(col0 + c8 * 8, ra);
-        tmem_ld8(col0 + 64 + c8 * 8, ia);
-        tmem_ld8(col0 + 32 + c8 * 8, rz);
-        tmem_ld8(col0 + 96 + c8 * 8, iz);
+    for (int r = 0; r < 4; ++r) {
+        uint32_t re[4][4], im[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            tmem_ld4(col0 + 16 * q + 4 * r, re[q]);
+            tmem_ld4(col0 + 64 + 16 * q + 4 * r, im[q]);
+        }
         tmem_wait_ld();
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            ea = cfma(k.lb, ea, make_float2(__uint_as_float(ra[t]), __uint_as_float(ia[t])));
-            ez = cfma(k.lb, ez, make_float2(__uint_as_float(rz[t]), __uint_as_float(iz[t])));
+        for (int t = 0; t < 4; ++t) {
+            c0 = cfma(k.lb, c0, make_float2(__uint_as_float(re[0][t]), __uint_as_float(im[0][t])));
+            c1 = cfma(k.lb, c1, make_float2(__uint_as_float(re[1][t]), __uint_as_float(im[1][t])));
+            c2 = cfma(k.lb, c2, make_float2(__uint_as_float(re[2][t]), __uint_as_float(im[2][t])));
+            c3 = cfma(k.lb, c3, make_float2(__uint_as_float(re[3][t]), __uint_as_float(im[3][t])));
         }
     }
-    elo = ea;
-    return cfma(k.lb32, ea, ez);
+    e[0] = c0;
+    e[1] = c1;
+    e[2] = c2;
+    return cfma(k.lb16, cfma(k.lb16, cfma(k.lb16, c0, c1), c2), c3);
 }
 
 // Short tile (Tc < 64): end state from zero over its Tc tokens.
-__device__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
+__device__ __noinline__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
     float2 e = make_float2(0.f, 0.f);
 #pragma unroll 1
     for (int ch = 0; ch * 16 < Tc; ++ch) {
@@ -333,35 +346,56 @@ __device__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
     return e;
 }
 
-// Full tile: states from the carry as two interleaved 32-step chains (the
-// second starts from lambda_bar^32 carry + elo), each written as bf16 (Re, Im)
-// into row t of X.  Returns the state after token 63.
+// Signals that this warp has finished reading the tile's Bu columns.
+__device__ __forceinline__ void bu_read_done(uint64_t *bar) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Full tile, pass 2: the four chains start from the carry S and
+// S_{q+1} = L S_q + e_q; every state goes as bf16 (Re, Im) into row t of X
+// (row t at xb[t & 7] + (t >> 3) * 1024).  `done` is arrived once the last
+// Bu column is in registers.  Returns the state after token 63.
 __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)[8], const ScanConsts &k,
-                                             float2 carry, float2 elo) {
-    float2 xa = carry, xz = cfma(k.lb32, carry, elo);
-#pragma unroll 1   // rolled: keeps the scan warps within their register budget
-    for (int c8 = 0; c8 < 4; ++c8) {
-        // tokens 8*c8 .. +7 (chain a) and 32 + 8*c8 .. +7 (chain z)
-        uint32_t ra[8], ia[8], rz[8], iz[8];
-        tmem_ld8(col0 + c8 * 8, ra);
-        tmem_ld8(col0 + 64 + c8 * 8, ia);
-        tmem_ld8(col0 + 32 + c8 * 8, rz);
-        tmem_ld8(col0 + 96 + c8 * 8, iz);
-        tmem_wait_ld();
+                                             float2 S, const float2 (&e)[3], uint64_t *done) {
+    float2 s0 = S;
+    float2 s1 = cfma(k.lb16, s0, e[0]);
+    float2 s2 = cfma(k.lb16, s1, e[1]);
+    float2 s3 = cfma(k.lb16, s2, e[2]);
+    // rounds of 4 tokens per chain (token 16q + 4r + t is row (2q + r/2) * 8 + (r%2)*4 + t)
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+        uint32_t re[4][4], im[4][4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            xa = cfma(k.lb, xa, make_float2(__uint_as_float(ra[t]), __uint_as_float(ia[t])));
-            xz = cfma(k.lb, xz, make_float2(__uint_as_float(rz[t]), __uint_as_float(iz[t])));
-            // row 8*c8 + t lives at xb[t] + c8 * 1024; row 32 + 8*c8 + t at xb[t] + (4 + c8) * 1024
-            sts32(xb[t] + (uint32_t)c8 * 1024u, pack_bf16(xa.x, xa.y));
-            sts32(xb[t] + (uint32_t)(4 + c8) * 1024u, pack_bf16(xz.x, xz.y));
+        for (int q = 0; q < 4; ++q) {
+            tmem_ld4(col0 + 16 * q + 4 * r, re[q]);
+            tmem_ld4(col0 + 64 + 16 * q + 4 * r, im[q]);
         }
+        tmem_wait_ld();
+        if (r == 3) bu_read_done(done);
+        const uint32_t o = (uint32_t)(r >> 1) * 1024u;
+        const int t0 = (r & 1) * 4;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            s0 = cfma(k.lb, s0, make_float2(__uint_as_float(re[0][t]), __uint_as_float(im[0][t])));
+            s1 = cfma(k.lb, s1, make_float2(__uint_as_float(re[1][t]), __uint_as_float(im[1][t])));
+            s2 = cfma(k.lb, s2, make_float2(__uint_as_float(re[2][t]), __uint_as_float(im[2][t])));
+            s3 = cfma(k.lb, s3, make_float2(__uint_as_float(re[3][t]), __uint_as_float(im[3][t])));
+            const uint32_t a = ((r & 1) ? xb[4 + t] : xb[t]) + o;
+            sts32(a, pack_bf16(s0.x, s0.y));
+            sts32(a + 2048u, pack_bf16(s1.x, s1.y));
+            sts32(a + 4096u, pack_bf16(s2.x, s2.y));
+            sts32(a + 6144u, pack_bf16(s3.x, s3.y));
+        }
+        (void)t0;
     }
-    return xz;
+    return s3;
 }
 
 // Short tile: sequential states; rows past Tc are written as zeros.
-__device__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb, float2 x, int Tc) {
+__device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb, float2 x, int Tc,
+                                            uint64_t *done) {
 #pragma unroll 1
     for (int ch = 0; ch < T_TOK / 16; ++ch) {
         uint32_t re[16], im[16];
@@ -381,13 +415,14 @@ __device__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb,
             sts32(xb[t & 7] + (uint32_t)((ch * 16 + t) >> 3) * 1024u, pv);
         }
     }
+    bu_read_done(done);
     return x;
 }
 
-// One tile in flight in the scan warps.
+// One tile in flight in the scan warps: its length and pass-1 chain states.
 struct ScanTile {
-    int g, b, c, Tc, r;
-    float2 elo;
+    int Tc;
+    float2 e[3];
 };
 
 // Pass 1 of local tile i: waits for its GEMM1, runs pass 1 and publishes the
@@ -395,16 +430,21 @@ struct ScanTile {
 __device__ __forceinline__ bool scan_front(ScanTile &T, int i, const Lane &ln, int L, uint32_t lane_base,
                                            const ScanConsts &kc, float4 *rec, int m, unsigned tag,
                                            unsigned drop, Bars *sb, WsHeader *hdr) {
-    ln.tile(i, T.b, T.c);
-    T.g = T.b * ln.nchunks + T.c;
-    T.Tc = min(T_TOK, L - T.c * T_TOK);
-    T.r = i % REGIONS;
-    if (!pipe_wait(&sb->tmem_full[T.r], (i / REGIONS) & 1, sb, hdr)) return false;
+    int b, c;
+    ln.tile(i, b, c);
+    const int g = b * ln.nchunks + c, r = i % REGIONS;
+    T.Tc = min(T_TOK, L - c * T_TOK);
+    if (!pipe_wait(&sb->tmem_full[r], (i / REGIONS) & 1, sb, hdr)) return false;
     tc_fence_after();
-    const uint32_t col0 = lane_base + (uint32_t)T.r * 128u;
-    T.elo = make_float2(0.f, 0.f);
-    const float2 E = (T.Tc == T_TOK) ? pass1_full(col0, kc, T.elo) : pass1_short(col0, T.Tc, kc.lb);
-    if (drop != (unsigned)T.g + 1u) st_record(rec + (size_t)T.g * P_M + m, E, tag);
+    const uint32_t col0 = lane_base + (uint32_t)r * 128u;
+    float2 E;
+    if (T.Tc == T_TOK) {
+        E = pass1_full(col0, kc, T.e);
+    } else {
+        E = pass1_short(col0, T.Tc, kc.lb);
+        T.e[0] = T.e[1] = T.e[2] = make_float2(0.f, 0.f);
+    }
+    if (drop != (unsigned)g + 1u) st_record(rec + (size_t)g * P_M + m, E, tag);
     return true;
 }
 
@@ -470,17 +510,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&sb->full_u[s], 1);
-                mbar_init(&sb->empty_u[s], 2);   // the two GEMM1 halves
+                mbar_init(&sb->empty_u[s], 1);     // GEMM1's commit
             }
             for (int r = 0; r < REGIONS; ++r) {
-                mbar_init(&sb->tmem_full[r], 2);   // the two GEMM1 halves
+                mbar_init(&sb->tmem_full[r], 1);   // GEMM1's commit
                 mbar_init(&sb->tmem_empty[r], 4);  // the four epilogue warps
-                mbar_init(&sb->mma2_done[r], 2);   // the two GEMM2 halves
+                mbar_init(&sb->p2read[r], 4);      // the four scan warps
+                mbar_init(&sb->mma2_done[r], 1);   // GEMM2's commit
             }
-            mbar_init(&sb->xready, 4);
-            mbar_init(&sb->xfree, 2);
+            mbar_init(&sb->xready, 4);             // the four scan warps
+            mbar_init(&sb->xfree, 1);              // GEMM2's commit
+            mbar_init(&sb->eu_full, 1);
+            mbar_init(&sb->eu_empty, 4);           // the four epilogue warps
             mbar_init(&sb->weights, 1);
-            mbar_init(&sb->drain, 4);          // the four issuing threads
+            mbar_init(&sb->drain, 2);          // the two MMA-issuing threads
             for (int q = 0; q < 2; ++q) {
                 mbar_init(&sb->carry_full[q], 4);    // the four fold warps
                 mbar_init(&sb->carry_empty[q], 4);   // the four scan warps
@@ -508,15 +551,29 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
 
     if (!pipeline) {
         // nothing to run: straight to the teardown
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ TMA + MMA issue
-        // One dependent chain of 8 MMAs per thread and tile: a single thread
-        // issues a chain of accumulating MMAs at roughly one per 235 cycles, so
-        // the tile's 32 MMAs are spread over four issuing threads.
-        //   warp 1: GEMM1 rows 0..P-1 (Re),  warp 2: GEMM1 rows P..2P-1 (Im),
-        //   warp 3: GEMM2 k-steps 0..7,      warp 0: GEMM2 k-steps 8..15 and the
-        //   TMA producer.  GEMM2's two halves accumulate into columns 0..63 and
-        //   64..127 of the tile's region; the epilogue adds them.
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ u for the epilogue
+        // A second TMA load of each tile's u, into the epilogue's buffer once
+        // the epilogue has read the previous tile's copy.
+        if (lane == 0) {
+            int last = -1;
+            for (int i = 0; i < n; ++i) {
+                if (i > 0 && !pipe_wait(&sb->eu_empty, (i - 1) & 1, sb, hdr)) break;
+                int b, c;
+                ln.tile(i, b, c);
+                mbar_arrive_tx(&sb->eu_full, U_STAGE);
+                tma_load_3d(smem + SM_EU, &tmap_u, 0, c * T_TOK, b, &sb->eu_full);
+                tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->eu_full);
+                last = i;
+            }
+            // the copy in flight must land before the CTA exits
+            if (last >= 0) drain_wait(&sb->eu_full, last & 1);
+        }
+    } else if (warp < 3) {
+        // ------------------------------------------------------------ TMA and MMA issue
+        // One thread each: warp 0 loads u tiles, warp 1 issues GEMM1, warp 2
+        // GEMM2.  A thread issues a chain of MMAs whose descriptors are
+        // compile-time offsets at close to the tensor pipe's rate.
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, T_TOK);
             const uint32_t bs = smem_addr(smem + SM_BS), cp = smem_addr(smem + SM_CP);
@@ -526,94 +583,91 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                 mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
                 bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
                 bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
-            }
-            bool ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
-            if (warp == 1 || warp == 2) {
-                const int mb = warp - 1;
-                for (int g = 0; ok && g < n; ++g) {
-                    const int s = g % STAGES, r = g % REGIONS;
-                    ok = pipe_wait(&sb->full_u[s], (g / STAGES) & 1, sb, hdr) &&
-                         (g < REGIONS || pipe_wait(&sb->tmem_empty[r], ((g / REGIONS) - 1) & 1, sb, hdr));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t ub = smem_addr(smem + SM_U + s * U_STAGE);
-#pragma unroll
-                    for (int kq = 0; kq < H_F / 16; ++kq)
-                        mma_bf16(tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u,
-                                 sw128_kmajor_desc(bs + (kq >> 2) * (2 * P_M * 128) + mb * (P_M * 128) + (kq & 3) * 32),
-                                 sw128_kmajor_desc(ub + (kq >> 2) * (T_TOK * 128) + (kq & 3) * 32), idesc, kq > 0);
-                    mma_commit(&sb->tmem_full[r]);
-                    mma_commit(&sb->empty_u[s]);
-                }
-            } else {
-                // GEMM2 half hf (and, in warp 0, the u loads)
-                const int hf = warp == 3 ? 0 : 1;
-                int g2 = 0, il = 0;   // next tile for GEMM2 / for a u load
                 int last_issue[STAGES];
                 for (int q = 0; q < STAGES; ++q) last_issue[q] = -1;
-                const int nl = warp == 0 ? n : 0;
-                unsigned long long t0 = global_ns();
-                while (ok && (g2 < n || il < nl)) {
-                    bool progress = false;
-                    if (il < nl) {
-                        const int s = il % STAGES;
-                        if (il < STAGES || mbar_test_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1)) {
-                            int b, c;
-                            ln.tile(il, b, c);
-                            unsigned char *dst = smem + SM_U + s * U_STAGE;
-                            mbar_arrive_tx(&sb->full_u[s], U_STAGE);
-                            tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
-                            tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
-                            last_issue[s] = il;
-                            ++il;
-                            progress = true;
-                        }
-                    }
-                    if (g2 < n && mbar_test_wait(&sb->xready, g2 & 1)) {
+                for (int il = 0; il < n; ++il) {
+                    const int s = il % STAGES;
+                    if (il >= STAGES && !pipe_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1, sb, hdr)) break;
+                    int b, c;
+                    ln.tile(il, b, c);
+                    unsigned char *dst = smem + SM_U + s * U_STAGE;
+                    mbar_arrive_tx(&sb->full_u[s], U_STAGE);
+                    tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
+                    tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
+                    last_issue[s] = il;
+                }
+                // copies still in flight must land before the CTA exits
+                drain_wait(&sb->weights, 0);
+                for (int q = 0; q < STAGES; ++q)
+                    if (last_issue[q] >= 0) drain_wait(&sb->full_u[q], (last_issue[q] / STAGES) & 1);
+            } else {
+                bool ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
+                if (warp == 1) {
+                    // GEMM1 of tile g into region g % REGIONS: Re rows into
+                    // columns 0..63, Im rows into 64..127.
+                    const uint64_t da = sw128_kmajor_desc(bs);
+                    for (int g = 0; ok && g < n; ++g) {
+                        const int s = g % STAGES, r = g % REGIONS;
+                        ok = pipe_wait(&sb->full_u[s], (g / STAGES) & 1, sb, hdr) &&
+                             (g < REGIONS || pipe_wait(&sb->tmem_empty[r], ((g / REGIONS) - 1) & 1, sb, hdr));
+                        if (!ok) break;
                         tc_fence_after();
-                        const uint32_t d = tmem + (uint32_t)(g2 % REGIONS) * 128u + (uint32_t)hf * 64u;
+                        // descriptors: a base plus compile-time offsets (a descriptor's
+                        // low bits hold the address / 16, and no offset carries out)
+                        const uint64_t db = sw128_kmajor_desc(smem_addr(smem + SM_U + s * U_STAGE));
+                        const uint32_t d0 = tmem + (uint32_t)r * 128u;
 #pragma unroll
-                        for (int k8 = 0; k8 < 8; ++k8) {
-                            const int kq = hf * 8 + k8;
-                            mma_bf16(d, sw128_kmajor_desc(cp + (kq >> 2) * (H_F * 128) + (kq & 3) * 32),
-                                     sw128_kmajor_desc(xs + (kq >> 2) * (T_TOK * 128) + (kq & 3) * 32), idesc,
-                                     k8 > 0);
+                        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                            for (int kq = 0; kq < H_F / 16; ++kq) {
+                                const uint64_t a = da + (uint64_t)(((kq >> 2) * (2 * P_M * 128) + mb * (P_M * 128) +
+                                                                    (kq & 3) * 32) >> 4);
+                                const uint64_t bb = db + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
+                                if (kq == 0)
+                                    mma_bf16_c<false>(d0 + (uint32_t)mb * 64u, a, bb, idesc);
+                                else
+                                    mma_bf16_c<true>(d0 + (uint32_t)mb * 64u, a, bb, idesc);
+                            }
+                        mma_commit(&sb->tmem_full[r]);
+                        mma_commit(&sb->empty_u[s]);
+                    }
+                } else {
+                    const uint64_t dc = sw128_kmajor_desc(cp), dx = sw128_kmajor_desc(xs);
+                    // GEMM2 of tile g into columns 0..63 of its region once X
+                    // is complete (the scan warps have also read the tile's
+                    // Bu by then): 16 MMAs back to back, since every wait or
+                    // commit between them lets the tensor pipe drain.
+                    for (int g = 0; ok && g < n; ++g) {
+                        const int r = g % REGIONS;
+                        ok = pipe_wait(&sb->xready, g & 1, sb, hdr);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t d = tmem + (uint32_t)r * 128u;
+#pragma unroll
+                        for (int kq = 0; kq < 16; ++kq) {
+                            const uint64_t a = dc + (uint64_t)(((kq >> 2) * (H_F * 128) + (kq & 3) * 32) >> 4);
+                            const uint64_t bb = dx + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
+                            if (kq == 0)
+                                mma_bf16_c<false>(d, a, bb, idesc);
+                            else
+                                mma_bf16_c<true>(d, a, bb, idesc);
                         }
-                        mma_commit(&sb->mma2_done[g2 % REGIONS]);
                         mma_commit(&sb->xfree);
-                        ++g2;
-                        progress = true;
-                    }
-                    if (progress) {
-                        t0 = global_ns();
-                    } else if (aborted(sb)) {
-                        break;
-                    } else if (global_ns() - t0 > PIPE_WAIT_NS) {
-                        set_abort(sb, hdr);
-                        break;
-                    } else {
-                        __nanosleep(32);
+                        mma_commit(&sb->mma2_done[r]);
                     }
                 }
-                if (warp == 0) {
-                    // copies still in flight must land before the CTA exits
-                    drain_wait(&sb->weights, 0);
-                    for (int q = 0; q < STAGES; ++q)
-                        if (last_issue[q] >= 0) drain_wait(&sb->full_u[q], (last_issue[q] / STAGES) & 1);
-                }
+                // every MMA issued must complete before TMEM is freed
+                mma_commit(&sb->drain);
+                drain_wait(&sb->drain, 0);
             }
-            // every MMA issued must complete before TMEM is freed
-            mma_commit(&sb->drain);
-            drain_wait(&sb->drain, 0);
         }
     } else if (warp >= W_SCAN && warp < W_SCAN + 4) {
         // ------------------------------------------------------------ scan
-        const int qd = warp - W_SCAN;           // TMEM lane quarter
+        const int qd = warp - W_SCAN;           // TMEM lane quarter = k-block of X
         const int m = 32 * qd + lane;
         ScanConsts kc;
         kc.lb = args.lambda_bar[m];
-        kc.lb32 = cpow(kc.lb, 32);
-        kc.lb64 = cmul(kc.lb32, kc.lb32);
+        kc.lb16 = cpow(kc.lb, 16);
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const uint32_t xcol = (uint32_t)lane * 4u;   // byte of (Re, Im) in this warp's k-block row
         // shared address of (row q, this lane's column) in each swizzle phase q;
@@ -626,47 +680,41 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         const float2 *slots = reinterpret_cast<const float2 *>(smem + SM_CARRY);
         const unsigned drop = sb->drop;
 
-        // Every exit from this loop is decided by named_bar_and, so the four
-        // warps always meet at the same barriers.
+        // Step j runs pass 1 of tile j, then pass 2 of tile j - 2.  Every exit
+        // from this loop is decided by named_bar_and, so the four warps always
+        // meet at the same barriers.
         ScanTile t0, t1, t2;
-        bool alive = true;
-        for (int j = 0; j < 2 && j < n; ++j) {
-            ScanTile &T = j == 0 ? t0 : t1;
-            const bool mine = scan_front(T, j, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
-            if (!named_bar_and(BAR_SCAN, 128, mine)) {
-                alive = false;
-                break;
-            }
-        }
         float2 xprev = make_float2(0.f, 0.f);
         bool mine = true;
-        for (int i = 0; alive && i < n; ++i) {
-            const bool front = i + 2 < n;
-            if (mine && front)
-                mine = scan_front(t2, i + 2, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
+        for (int j = 0; j < n + 2; ++j) {
+            if (mine && j < n) mine = scan_front(t2, j, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
             if (!named_bar_and(BAR_SCAN, 128, mine)) break;
-            // carry of tile i: from the carry warps' slot, or (one lane per
-            // sequence) the previous tile's end state
-            float2 carry = xprev;
-            if (W > 1) {
-                mine = pipe_wait(&sb->carry_full[i & 1], (i >> 1) & 1, sb, hdr);
-                if (mine) {
-                    carry = slots[(i & 1) * P_M + m];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sb->carry_empty[i & 1]);
+            const int i = j - 2;
+            if (i >= 0) {
+                // carry of tile i: from the carry warps' slot, or (one lane per
+                // sequence) the previous tile's end state
+                int b0, c0;
+                ln.tile(i, b0, c0);
+                const int r0 = i % REGIONS;
+                float2 carry = xprev;
+                if (W > 1) {
+                    mine = pipe_wait(&sb->carry_full[i & 1], (i >> 1) & 1, sb, hdr);
+                    if (mine) {
+                        carry = slots[(i & 1) * P_M + m];
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sb->carry_empty[i & 1]);
+                    }
+                } else if (c0 == 0) {
+                    carry = args.x0 ? args.x0[(size_t)b0 * P_M + m] : make_float2(0.f, 0.f);
                 }
-            } else if (t0.c == 0) {
-                carry = args.x0 ? args.x0[(size_t)t0.b * P_M + m] : make_float2(0.f, 0.f);
-            }
-            if (mine) {
-                // pass 2 of tile i once GEMM2 of tile i-1 has read X
-                mine = i == 0 || pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr);
+                // pass 2 once GEMM2 of tile i-1 has read X
+                if (mine) mine = i == 0 || pipe_wait(&sb->xfree, (i - 1) & 1, sb, hdr);
                 if (mine) {
                     tc_fence_after();
-                    const uint32_t col0 = lane_base + (uint32_t)t0.r * 128u;
-                    xprev = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, carry, t0.elo)
-                                             : pass2_short(col0, xb, kc.lb, carry, t0.Tc);
-                    if (t0.c == nchunks - 1 && args.x_last) args.x_last[(size_t)t0.b * P_M + m] = xprev;
+                    const uint32_t col0 = lane_base + (uint32_t)r0 * 128u;
+                    xprev = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, carry, t0.e, &sb->p2read[r0])
+                                             : pass2_short(col0, xb, kc.lb, carry, t0.Tc, &sb->p2read[r0]);
+                    if (c0 == nchunks - 1 && args.x_last) args.x_last[(size_t)b0 * P_M + m] = xprev;
                     fence_proxy_async_smem();
                     tc_fence_before();
                     __syncwarp();
@@ -678,47 +726,53 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         }
     } else if (warp >= W_EPI && warp < W_EPI + 4) {
         // ------------------------------------------------------------ epilogue
+        // thread = feature h = TMEM lane of GEMM2: y = acc + D * u over the
+        // tile's tokens.  The tile's u is loaded before waiting for GEMM2 and
+        // left untouched until after the wait (no instruction depends on the
+        // loads before then), so their latency overlaps the wait; the region
+        // is released once its last column is in registers.
         const int qd = warp - W_EPI;
         const int h = 32 * qd + lane;
         const float dh = args.d[h];
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        const __nv_bfloat16 *uin = static_cast<const __nv_bfloat16 *>(args.u);
-        __nv_bfloat16 *yout = static_cast<__nv_bfloat16 *>(args.y);
+        unsigned short *yout = static_cast<unsigned short *>(args.y);
+        // this feature's u for token t: row t, column h of the swizzled copy
+        const unsigned char *eu = smem + SM_EU + (h >> 6) * (T_TOK * 128);
+        const uint32_t hc = (uint32_t)(h & 63);
         for (int i = 0; i < n; ++i) {
             const int r = i % REGIONS;
             int b, c;
             ln.tile(i, b, c);
             const int Tc = min(T_TOK, L - c * T_TOK);
             const size_t row0 = ((size_t)b * L + (size_t)c * T_TOK) * H_F + h;
-            // this feature's u over the tile, loaded before the wait so that
-            // the latency overlaps it
-            __nv_bfloat16 uv[T_TOK];
+            unsigned short *yrow = yout + row0;
+            if (!pipe_wait(&sb->eu_full, i & 1, sb, hdr)) break;
+            unsigned short uv[T_TOK];
 #pragma unroll
-            for (int k = 0; k < T_TOK; ++k)
-                uv[k] = (k < Tc) ? uin[row0 + (size_t)k * H_F] : __float2bfloat16_rn(0.f);
+            for (int t = 0; t < T_TOK; ++t)
+                uv[t] = *reinterpret_cast<const unsigned short *>(eu + t * 128 + ((((hc >> 3) ^ (uint32_t)(t & 7))) << 4) +
+                                                                  ((hc & 7u) << 1));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sb->eu_empty);
             if (!pipe_wait(&sb->mma2_done[r], (i / REGIONS) & 1, sb, hdr)) break;
             tc_fence_after();
-            __nv_bfloat16 *yrow = yout + row0;
 #pragma unroll
-            for (int ch = 0; ch < T_TOK / 16; ++ch) {
-                uint32_t ya[16], yb[16];
-                tmem_ld16(lane_base + (uint32_t)r * 128u + ch * 16, ya);
-                tmem_ld16(lane_base + (uint32_t)r * 128u + 64u + ch * 16, yb);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t ya[32];
+                tmem_ld32(lane_base + (uint32_t)r * 128u + (uint32_t)hf * 32u, ya);
                 tmem_wait_ld();
-                float yv[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) yv[k] = __uint_as_float(ya[k]) + __uint_as_float(yb[k]);
-                if (ch == 3) {
+                if (hf == 1) {
                     // every column of the region has been read: it may be reused
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sb->tmem_empty[r]);
                 }
 #pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    if (ch * 16 + k < Tc)
-                        yrow[(size_t)(ch * 16 + k) * H_F] =
-                            __float2bfloat16_rn(fmaf(dh, __bfloat162float(uv[ch * 16 + k]), yv[k]));
+                for (int k = 0; k < 32; ++k) {
+                    const int t = hf * 32 + k;
+                    const float v = fmaf(dh, __uint_as_float((uint32_t)uv[t] << 16), __uint_as_float(ya[k]));
+                    if (t < Tc) yrow[(size_t)t * H_F] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                }
             }
         }
     } else if (warp >= W_FOLD && warp < W_FOLD + 4 && W > 1) {
