@@ -26,62 +26,57 @@ __device__ inline dcplx ddiv(dcplx a, dcplx b) {
 }
 
 // One block per mode (float64 throughput per SM is small, so the work is
-// spread over P SMs).  The float64 functions of the mode's factors are spread
-// over the first four threads, so that each evaluates at most two of them in
-// sequence:
+// spread over P SMs).  The float64 functions of the mode's factors run side by
+// side on the first lane of four different warps (lanes of one warp taking
+// different branches would run them one after another):
 //   every thread  dt = exp(log_dt)
-//   thread 0      sin(Im z), cos(Im z)      thread 1  exp(Re z)
-//   thread 2      expm1(Re z)               thread 3  sin(Im z / 2)
+//   warp 0  sin(Im z), cos(Im z)      warp 1  exp(Re z)
+//   warp 2  expm1(Re z)               warp 3  sin(Im z / 2)
 // then lambda_bar = e^Re z (cos, sin) and, for |z| >= 1e-4,
 // (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z))/lambda;
 // below |z| = 1e-4, Delta * phi1(z) from its Taylor series.  Every thread of
-// the block then scales a slice of the B_tilde row.
+// the block then scales a slice of the B_tilde row.  Blocks have >= 128 threads.
 __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float *__restrict__ log_dt,
                                   const float2 *__restrict__ b_tilde, int P, int H,
                                   float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar) {
     const int p = blockIdx.x;
+    __shared__ double s_f[5];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2)
     __shared__ double s_gain[2];
-    if (threadIdx.x < 32) {
-        const int q = threadIdx.x & 3;
-        const float2 l = lambda[p];
-        const dcplx lam = {(double)l.x, (double)l.y};
-        const double dt = exp((double)log_dt[p]);
-        const dcplx z = {lam.re * dt, lam.im * dt};
-        double f0 = 0.0, f1 = 0.0;
-        if (threadIdx.x < 4) {
-            if (q == 0) sincos(z.im, &f0, &f1);
-            else if (q == 1) f0 = exp(z.re);
-            else if (q == 2) f0 = expm1(z.re);
-            else f0 = sin(0.5 * z.im);
-        }
-        const unsigned full = 0xffffffffu;
-        const double s = __shfl_sync(full, f0, 0), c = __shfl_sync(full, f1, 0);
-        const double mag = __shfl_sync(full, f0, 1);
-        const double em1r = __shfl_sync(full, f0, 2);
-        const double sh = __shfl_sync(full, f0, 3);
-        if (threadIdx.x == 0) {
-            dcplx gain;
-            const double zabs = sqrt(z.re * z.re + z.im * z.im);
-            if (zabs < 1e-4) {
-                // dt * (1 + z/2 + z^2/6 + z^3/24 + z^4/120); the next term is below 1e-22.
-                dcplx term = {1.0, 0.0}, phi = {1.0, 0.0};
-                for (int n = 1; n <= 4; ++n) {
-                    term = dmul(term, z);
-                    const double f = 1.0 / (double)(n + 1);
-                    term.re *= f;
-                    term.im *= f;
-                    phi.re += term.re;
-                    phi.im += term.im;
-                }
-                gain = {dt * phi.re, dt * phi.im};
-            } else {
-                const dcplx em1 = {em1r * c - 2.0 * sh * sh, mag * s};
-                gain = ddiv(em1, lam);
+    const float2 l = lambda[p];
+    const dcplx lam = {(double)l.x, (double)l.y};
+    const double dt = exp((double)log_dt[p]);
+    const dcplx z = {lam.re * dt, lam.im * dt};
+    if ((threadIdx.x & 31) == 0) {
+        const int w = threadIdx.x >> 5;
+        if (w == 0) sincos(z.im, &s_f[0], &s_f[1]);
+        else if (w == 1) s_f[2] = exp(z.re);
+        else if (w == 2) s_f[3] = expm1(z.re);
+        else if (w == 3) s_f[4] = sin(0.5 * z.im);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const double s = s_f[0], c = s_f[1], mag = s_f[2], em1r = s_f[3], sh = s_f[4];
+        dcplx gain;
+        const double zabs = sqrt(z.re * z.re + z.im * z.im);
+        if (zabs < 1e-4) {
+            // dt * (1 + z/2 + z^2/6 + z^3/24 + z^4/120); the next term is below 1e-22.
+            dcplx term = {1.0, 0.0}, phi = {1.0, 0.0};
+            for (int n = 1; n <= 4; ++n) {
+                term = dmul(term, z);
+                const double f = 1.0 / (double)(n + 1);
+                term.re *= f;
+                term.im *= f;
+                phi.re += term.re;
+                phi.im += term.im;
             }
-            lambda_bar[p] = make_float2((float)(mag * c), (float)(mag * s));
-            s_gain[0] = gain.re;
-            s_gain[1] = gain.im;
+            gain = {dt * phi.re, dt * phi.im};
+        } else {
+            const dcplx em1 = {em1r * c - 2.0 * sh * sh, mag * s};
+            gain = ddiv(em1, lam);
         }
+        lambda_bar[p] = make_float2((float)(mag * c), (float)(mag * s));
+        s_gain[0] = gain.re;
+        s_gain[1] = gain.im;
     }
     __syncthreads();
     const dcplx g = {s_gain[0], s_gain[1]};
@@ -118,7 +113,7 @@ __global__ void mode_consts_kernel(const float2 *__restrict__ lambda, const floa
 
 cudaError_t launch_discretize(const float2 *lambda, const float *log_dt, const float2 *b_tilde,
                               int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st) {
-    const int threads = H >= 256 ? 256 : (H >= 128 ? 128 : 64);
+    const int threads = H >= 256 ? 256 : 128;   // at least four warps (see discretize_kernel)
     discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar);
     return cudaGetLastError();
 }

@@ -627,11 +627,13 @@ __global__ void zoh_chain_kernel(const float2 *__restrict__ lambda, const float 
     const dc lam = {(double)l.x, (double)l.y};
     const double dt = exp((double)log_dt[p]);
     const dc z = {lam.re * dt, lam.im * dt};
-    // the four fp64 transcendentals side by side, one thread each
+    // the four fp64 transcendentals side by side, on the first lane of four
+    // different warps (lanes of one warp on different branches would run
+    // them one after another); the block has 128 threads
     if (threadIdx.x == 0) sincos(z.im, &s_tr[0], &s_tr[1]);
-    else if (threadIdx.x == 1) s_tr[2] = exp(z.re);
-    else if (threadIdx.x == 2) s_tr[3] = expm1(z.re);
-    else if (threadIdx.x == 3) s_tr[4] = sin(0.5 * z.im);
+    else if (threadIdx.x == 32) s_tr[2] = exp(z.re);
+    else if (threadIdx.x == 64) s_tr[3] = expm1(z.re);
+    else if (threadIdx.x == 96) s_tr[4] = sin(0.5 * z.im);
     __syncthreads();
     if (threadIdx.x == 0) {
         const double zabs = sqrt(z.re * z.re + z.im * z.im);
