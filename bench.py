@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "S5 layer fwd tokens/s (batch*L/s) and fraction of HBM/tensor roofline"
+BIDI_METRIC = "S5 bidirectional layer fwd tokens/s (batch*L/s) and fraction of HBM/tensor roofline"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -41,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="pathx_bf16",
-                    choices=["small", "fp32", "pathx_bf16", "irregular", "stack6"])
+                    choices=["small", "fp32", "pathx_bf16", "pathx_bf16_bidir", "irregular", "stack6"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -146,6 +147,8 @@ def algorithmic_bytes(w, u_bytes_per, y_bytes_per):
     params = 8 * w.P + 8 * w.P * w.H * 2 + 4 * w.H
     if w.varying_dt:
         params += 4 * w.P + 4 * w.B * w.L      # log_dt and the gaps
+    if w.bidirectional:
+        params += 8 * w.P * w.H                # the backward half of C~
     return w.B * w.L * w.H * (u_bytes_per + y_bytes_per) + params
 
 
@@ -169,12 +172,17 @@ def run_ours(args):
     lam, log_dt = dev(inp["lambda_"]), dev(inp["log_dt"])
     bt, ct, d = dev(inp["b_tilde"]), dev(inp["c_tilde"]), dev(inp["d"])
     g = dev(inp["g"]) if w.varying_dt else None
+    ct2 = dev(inp["c_tilde2"]) if w.bidirectional else None
     NSETS = 4
     u_sets = [dev(inp["u"]).to(u_dt) for _ in range(NSETS)]
     y_sets = [torch.empty_like(u_sets[0]) for _ in range(NSETS)]
     lb = torch.empty(w.P, dtype=torch.complex64, device="cuda")
     bb = torch.empty(w.P, w.H, dtype=torch.complex64, device="cuda")
-    ws = api.new_workspace(w.B, w.L, w.H, w.P)
+    if w.bidirectional:
+        ws = torch.zeros(api.s5_bidirectional_workspace_size(w.B, w.L, w.H, w.P, u_dt, u_dt),
+                         dtype=torch.uint8, device="cuda")
+    else:
+        ws = api.new_workspace(w.B, w.L, w.H, w.P)
     stream = torch.cuda.current_stream()
 
     tc_path = (w.u_dtype == "bf16" and w.proj_dtype == "bf16" and w.H == 128 and w.P == 128
@@ -197,6 +205,8 @@ def run_ours(args):
         if w.varying_dt:
             api.s5_forward_varying_dt(lam, log_dt, bt, ct, d, g, u, y=y, proj_dtype=w.proj_dtype,
                                       workspace=ws)
+        elif w.bidirectional:
+            api.s5_forward_bidirectional(lb, bb, ct2, d, u, y=y, proj_dtype=w.proj_dtype, workspace=ws)
         else:
             api.s5_forward(lb, bb, ct, d, u, y=y, proj_dtype=w.proj_dtype, workspace=ws)
         if timed:
@@ -262,7 +272,8 @@ def run_ours(args):
     u_host = torch.from_numpy(np.ascontiguousarray(inp["u"])).to(u_dt).pin_memory()
     y_host = torch.empty(u_host.shape, dtype=u_dt).pin_memory()
     host_params = [torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
-                   for k in ("lambda_", "log_dt", "b_tilde", "c_tilde", "d")]
+                   for k in ("lambda_", "log_dt", "b_tilde",
+                             "c_tilde2" if w.bidirectional else "c_tilde", "d")]
     if w.varying_dt:
         host_params.append(torch.from_numpy(np.ascontiguousarray(inp["g"])).pin_memory())
     dev_params = [torch.empty_like(p, device="cuda") for p in host_params]
@@ -277,8 +288,12 @@ def run_ours(args):
                                       proj_dtype=w.proj_dtype, workspace=ws)
         else:
             l_, b_ = api.s5_discretize(dev_params[0], dev_params[1], dev_params[2], lb, bb)
-            api.s5_forward(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
-                           proj_dtype=w.proj_dtype, workspace=ws)
+            if w.bidirectional:
+                api.s5_forward_bidirectional(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
+                                             proj_dtype=w.proj_dtype, workspace=ws)
+            else:
+                api.s5_forward(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
+                               proj_dtype=w.proj_dtype, workspace=ws)
         y_host.copy_(y_dev, non_blocking=True)
 
     for _ in range(3):
@@ -314,8 +329,14 @@ def run_ours(args):
     kname = "fwd_tc_kernel" if tc_path else "fwd_simt_kernel"
     src = os.path.join(ROOT, "diagonal_state_space_gb300", "csrc",
                        "s5_forward_tc.cu" if tc_path else "s5_forward_simt.cu")
+    traffic = traffic_for(kname, src)
+    if w.bidirectional:
+        # the timed call is the whole bidirectional layer: two forward launches
+        # plus the split / reverse / add kernels; no single-kernel DRAM capture
+        kname = "bidirectional layer (2 x %s + split, reverse, add)" % kname
+        traffic = None
     result = {
-        "metric": METRIC,
+        "metric": BIDI_METRIC if w.bidirectional else METRIC,
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
@@ -329,12 +350,14 @@ def run_ours(args):
         "data": "synthetic (seeded numpy PCG64: u~N(0,1), lambda=-1/2+i*pi*n, "
                 "log_dt~U[ln1e-3,ln1e-1], B~,C~~CN(0,1/H), D~N(0,1))",
         "config": {
-            "workload": "%s: S5 layer forward, B=%d L=%d H=%d P=%d (stored complex modes), "
+            "workload": "%s: S5 %slayer forward, B=%d L=%d H=%d P=%d (stored complex modes), "
                         "u/y %s, proj %s, complex fp32 scan%s" % (
-                            w.name, w.B, w.L, w.H, w.P, w.u_dtype, w.proj_dtype,
-                            ", per-step interval" if w.varying_dt else ""),
+                            w.name, "bidirectional " if w.bidirectional else "", w.B, w.L, w.H, w.P,
+                            w.u_dtype, w.proj_dtype, ", per-step interval" if w.varying_dt else ""),
             "global_batch": w.B * world, "seq_len": w.L, "H": w.H, "P": w.P,
-            "step": ("s5_forward_varying_dt" if w.varying_dt else "s5_discretize + s5_forward"),
+            "step": ("s5_forward_varying_dt" if w.varying_dt else
+                     "s5_discretize + s5_forward_bidirectional" if w.bidirectional else
+                     "s5_discretize + s5_forward"),
             "arithmetic": ("bf16 tensor-core projections (fp32 accumulate), complex fp32 scan"
                            if tc_path else "fp32 CUDA-core projections, complex fp32 scan"),
             "timing": "K steps captured in one CUDA graph, replayed once between events",
@@ -353,14 +376,15 @@ def run_ours(args):
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
             "algorithmic_bytes_per_launch": alg,
             "launch_us": fwd_avg_s * 1e6,
-            "traffic": traffic_for(kname, src),
+            "traffic": traffic,
         },
         "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         # per step: discretize + (weight images + tensor-core forward | CUDA-core forward),
         # or, with per-step intervals, mode constants + CUDA-core forward
-        "gpu_launches": args.steps * (3 if tc_path else 2),
+        # bidirectional: discretize, split, reverse, 2 x (images + forward | forward), add
+        "gpu_launches": args.steps * ((8 if tc_path else 6) if w.bidirectional else (3 if tc_path else 2)),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -543,6 +567,8 @@ def oracle_run(w, inp, seqs):
         return oracle.forward_varying_dt(inp["lambda_"], inp["log_dt"], inp["b_tilde"],
                                          inp["c_tilde"], inp["d"], inp["g"][seqs], inp["u"][seqs])
     lb, bb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    if w.bidirectional:
+        return oracle.forward_bidirectional(lb, bb, inp["c_tilde2"], inp["d"], inp["u"][seqs])
     return oracle.forward(lb, bb, inp["c_tilde"], inp["d"], inp["u"][seqs])
 
 
@@ -578,7 +604,8 @@ def run_reference(args):
     dt = (time.perf_counter() - t0) / steps
     v = len(seqs) * w.L / dt
     sample = "%d sequence x %d tokens per step (of %d sequences)" % (len(seqs), w.L, w.B)
-    res = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+    res = {"metric": BIDI_METRIC if w.bidirectional else METRIC, "value": v, "unit": "tokens/s",
+           "n_gpus": world, "steps": steps,
            "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P,

@@ -23,6 +23,10 @@ SIGNATURES = {
     "s5_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                 _vp, _vp]),
     "s5_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "s5_discretize_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]),
+    "s5_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "s5_forward_bidirectional": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "s5_bidirectional_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "s5_sync_status": (_i, [_vp, _vp]),
     "s5_status_string": (ctypes.c_char_p, [_i]),
     "s5_last_cuda_error": (ctypes.c_char_p, []),

@@ -68,6 +68,77 @@ def s5_discretize(lam, log_dt, b_tilde, lambda_bar=None, b_bar=None, stream=None
     return lambda_bar, b_bar
 
 
+_METHOD = {"zoh": 0, "bilinear": 1}
+
+
+def s5_discretize_ex(lam, log_dt, b_tilde, method="zoh", clip_re=0.0, dt_scale=1.0, lambda_bar=None,
+                     b_bar=None, stream=None):
+    """Discretisation with options: method "zoh" or "bilinear", clip_eigs
+    threshold clip_re (0 = none; the official value is -1e-4), sampling-rate
+    factor dt_scale = old rate / new rate.  Returns (lambda_bar, b_bar)."""
+    P, H = b_tilde.shape
+    if lambda_bar is None:
+        lambda_bar = torch.empty(P, dtype=torch.complex64, device=b_tilde.device)
+    if b_bar is None:
+        b_bar = torch.empty(P, H, dtype=torch.complex64, device=b_tilde.device)
+    c64 = torch.complex64
+    code = _native.lib().s5_discretize_ex(
+        _ptr(lam, "lambda", c64, (P,)), _ptr(log_dt, "log_dt", torch.float32, (P,)),
+        _ptr(b_tilde, "b_tilde", c64), P, H, _METHOD[method], float(clip_re), float(dt_scale),
+        _ptr(lambda_bar, "lambda_bar", c64, (P,)), _ptr(b_bar, "b_bar", c64, (P, H)), _stream(stream))
+    check("s5_discretize_ex", code)
+    return lambda_bar, b_bar
+
+
+def s5_step(lambda_bar, b_bar, c_tilde, d, x, u, y=None, stream=None):
+    """One streaming step: x [B,P] complex64 is updated in place; returns y [B,H]."""
+    P, H = b_bar.shape
+    Bn = u.shape[0]
+    if y is None:
+        y = torch.empty(Bn, H, dtype=torch.float32, device=u.device)
+    c64 = torch.complex64
+    code = _native.lib().s5_step(
+        _ptr(lambda_bar, "lambda_bar", c64, (P,)), _ptr(b_bar, "b_bar", c64, (P, H)),
+        _ptr(c_tilde, "c_tilde", c64, (H, P)), _ptr(d, "d", torch.float32, (H,)),
+        _ptr(x, "x", c64, (Bn, P)), _ptr(u, "u", torch.float32, (Bn, H)),
+        _ptr(y, "y", torch.float32, (Bn, H)), Bn, H, P, _stream(stream))
+    check("s5_step", code)
+    return y
+
+
+def s5_bidirectional_workspace_size(B, L, H, P, u_dtype=torch.float32, y_dtype=None) -> int:
+    y_dtype = u_dtype if y_dtype is None else y_dtype
+    return int(_native.lib().s5_bidirectional_workspace_size(B, L, H, P, _DT[u_dtype], _DT[y_dtype]))
+
+
+def s5_forward_bidirectional(lambda_bar, b_bar, c_tilde2, d, u, y=None, y_dtype=None, proj_dtype="f32",
+                             workspace=None, stream=None):
+    """Bidirectional S5 layer: c_tilde2 [H,2P] holds the forward modes' C~ in
+    columns 0..P-1 and the backward modes' in P..2P-1.  Returns y."""
+    P = b_bar.shape[0]
+    Bn, L, H = u.shape
+    if u.dtype not in _DT:
+        raise ValueError("u must be float32 or bfloat16")
+    ydt = u.dtype if y_dtype is None else y_dtype
+    if isinstance(ydt, str):
+        ydt = {"f32": torch.float32, "bf16": torch.bfloat16}[ydt]
+    if y is None:
+        y = torch.empty(Bn, L, H, dtype=ydt, device=u.device)
+    if workspace is None:
+        n = s5_bidirectional_workspace_size(Bn, L, H, P, u.dtype, y.dtype)
+        if n == 0:
+            raise ValueError("invalid sizes for a workspace")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=u.device)
+    c64 = torch.complex64
+    code = _native.lib().s5_forward_bidirectional(
+        _ptr(lambda_bar, "lambda_bar", c64, (P,)), _ptr(b_bar, "b_bar", c64, (P, H)),
+        _ptr(c_tilde2, "c_tilde2", c64, (H, 2 * P)), _ptr(d, "d", torch.float32, (H,)),
+        _ptr(u, "u"), _DT[u.dtype], _ptr(y, "y", None, (Bn, L, H)), _DT[y.dtype], _DT_NAME[proj_dtype],
+        Bn, L, H, P, _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    check("s5_forward_bidirectional", code)
+    return y
+
+
 def _fwd_common(u, y, y_dtype, proj_dtype, x0, x_last, workspace, P):
     Bn, L, H = u.shape
     if u.dtype not in _DT:
@@ -151,6 +222,7 @@ def s5_sync_status(workspace, stream=None) -> int:
                                             _stream(stream)))
 
 
-__all__ = ["s5_discretize", "s5_forward", "s5_forward_varying_dt", "s5_forward_noalloc",
-           "s5_workspace_size",
-           "s5_sync_status", "new_workspace", "S5Error", "S5_F32", "S5_BF16"]
+__all__ = ["s5_discretize", "s5_discretize_ex", "s5_forward", "s5_forward_varying_dt",
+           "s5_forward_bidirectional", "s5_step", "s5_forward_noalloc", "s5_workspace_size",
+           "s5_bidirectional_workspace_size", "s5_sync_status", "new_workspace", "S5Error", "S5_F32",
+           "S5_BF16"]

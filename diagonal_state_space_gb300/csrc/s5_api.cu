@@ -11,8 +11,14 @@
 
 namespace s5 {
 cudaError_t launch_discretize(const float2 *, const float *, const float2 *, int, int, float2 *,
-                              float2 *, cudaStream_t);
+                              float2 *, cudaStream_t, int method = 0, double clip_re = 0.0, double dt_scale = 1.0);
 cudaError_t launch_mode_consts(const float2 *, const float *, int, ModeConst *, cudaStream_t);
+size_t step_smem_bytes(int H, int P);
+cudaError_t launch_step(const float2 *, const float2 *, const float2 *, const float *, float2 *, const float *,
+                        float *, int B, int H, int P, cudaStream_t);
+cudaError_t launch_split_c(const float2 *, int H, int P, float2 *, float2 *, cudaStream_t);
+cudaError_t launch_reverse_time(const void *, void *, int B, int L, int H, int elem_bytes, cudaStream_t);
+cudaError_t launch_add_reversed(void *, const void *, int B, int L, int H, bool bf16, cudaStream_t);
 }  // namespace s5
 
 namespace {
@@ -183,6 +189,22 @@ s5_status s5_discretize(const float *lambda, const float *log_dt, const float *b
     return e == cudaSuccess ? S5_OK : cuda_fail(e);
 }
 
+s5_status s5_discretize_ex(const float *lambda, const float *log_dt, const float *b_tilde, int P, int H,
+                           s5_discretization method, float clip_re, float dt_scale, float *lambda_bar,
+                           float *b_bar, s5_stream_t stream) {
+    if (P < 1 || H < 1) return S5_ERR_INVALID_ARGUMENT;
+    if (method != S5_ZOH && method != S5_BILINEAR) return S5_ERR_INVALID_ARGUMENT;
+    if (!(dt_scale > 0.f) || !(clip_re <= 0.f)) return S5_ERR_INVALID_ARGUMENT;   // also rejects NaN
+    const void *ptrs[] = {lambda, log_dt, b_tilde, lambda_bar, b_bar};
+    for (const void *p : ptrs)
+        if (!p || !aligned16(p)) return S5_ERR_INVALID_ARGUMENT;
+    cudaError_t e = s5::launch_discretize(
+        reinterpret_cast<const float2 *>(lambda), log_dt, reinterpret_cast<const float2 *>(b_tilde),
+        P, H, reinterpret_cast<float2 *>(lambda_bar), reinterpret_cast<float2 *>(b_bar),
+        reinterpret_cast<cudaStream_t>(stream), (int)method, (double)clip_re, (double)dt_scale);
+    return e == cudaSuccess ? S5_OK : cuda_fail(e);
+}
+
 s5_status s5_forward(const float *lambda_bar, const float *b_bar, const float *c_tilde,
                      const float *d, const void *u, s5_dtype u_dtype, void *y, s5_dtype y_dtype,
                      s5_dtype proj_dtype, int B, int L, int H, int P, const float *x0,
@@ -230,6 +252,83 @@ s5_status s5_forward_varying_dt(const float *lambda, const float *log_dt, const 
     return run_simt(nullptr, reinterpret_cast<const float2 *>(b_tilde),
                     reinterpret_cast<const float2 *>(c_tilde), d, dt_scale, u, u_dtype, y,
                     y_dtype, B, L, H, P, x0, x_last, workspace, true, st);
+}
+
+s5_status s5_step(const float *lambda_bar, const float *b_bar, const float *c_tilde, const float *d,
+                  float *x, const float *u, float *y, int B, int H, int P, s5_stream_t stream) {
+    if (B < 0 || H < 1 || P < 1) return S5_ERR_INVALID_ARGUMENT;
+    const void *params[] = {lambda_bar, b_bar, c_tilde, d};
+    for (const void *p : params)
+        if (!p || !aligned16(p)) return S5_ERR_INVALID_ARGUMENT;
+    if (B == 0) return S5_OK;
+    const void *io[] = {x, u, y};
+    for (const void *p : io)
+        if (!p || !aligned16(p)) return S5_ERR_INVALID_ARGUMENT;
+    if (s5::step_smem_bytes(H, P) > 48 * 1024) return S5_ERR_UNSUPPORTED;
+    cudaError_t e = s5::launch_step(reinterpret_cast<const float2 *>(lambda_bar), reinterpret_cast<const float2 *>(b_bar),
+                                    reinterpret_cast<const float2 *>(c_tilde), d, reinterpret_cast<float2 *>(x), u, y,
+                                    B, H, P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? S5_OK : cuda_fail(e);
+}
+
+// Bidirectional workspace: the forward workspace, then (each 256-aligned) the
+// time-reversed u, the backward scan's output, the two halves of c_tilde2 and
+// a zero d.
+struct BidiLayout {
+    size_t fwd, ur, yr, cf, cb, d0, total;
+};
+static BidiLayout bidi_layout(int B, int L, int H, int P, s5_dtype u_dtype, s5_dtype y_dtype) {
+    BidiLayout l{};
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t nel = (size_t)B * L * H;
+    l.fwd = al(s5_workspace_size(B, L, H, P));
+    l.ur = l.fwd;
+    l.yr = l.ur + al(nel * (u_dtype == S5_BF16 ? 2 : 4));
+    l.cf = l.yr + al(nel * (y_dtype == S5_BF16 ? 2 : 4));
+    l.cb = l.cf + al(sizeof(float) * 2 * (size_t)H * P);
+    l.d0 = l.cb + al(sizeof(float) * 2 * (size_t)H * P);
+    l.total = l.d0 + al(sizeof(float) * (size_t)H);
+    return l;
+}
+
+size_t s5_bidirectional_workspace_size(int B, int L, int H, int P, s5_dtype u_dtype, s5_dtype y_dtype) {
+    if (B < 0 || L < 0 || H < 1 || P < 1 || !dtype_ok(u_dtype) || !dtype_ok(y_dtype)) return 0;
+    if (s5_workspace_size(B, L, H, P) == 0) return 0;
+    return bidi_layout(B, L, H, P, u_dtype, y_dtype).total;
+}
+
+s5_status s5_forward_bidirectional(const float *lambda_bar, const float *b_bar, const float *c_tilde2,
+                                   const float *d, const void *u, s5_dtype u_dtype, void *y,
+                                   s5_dtype y_dtype, s5_dtype proj_dtype, int B, int L, int H, int P,
+                                   void *workspace, size_t workspace_bytes, s5_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!lambda_bar || !b_bar || !aligned16(lambda_bar) || !aligned16(b_bar)) return S5_ERR_INVALID_ARGUMENT;
+    if (B < 0 || L < 0 || H < 1 || P < 1) return S5_ERR_INVALID_ARGUMENT;
+    if (!dtype_ok(u_dtype) || !dtype_ok(y_dtype) || !dtype_ok(proj_dtype)) return S5_ERR_INVALID_ARGUMENT;
+    if (!c_tilde2 || !d || !aligned16(c_tilde2) || !aligned16(d)) return S5_ERR_INVALID_ARGUMENT;
+    if ((long long)B * L == 0) return S5_OK;
+    if (!u || !y || !aligned16(u) || !aligned16(y) || !workspace || !aligned16(workspace))
+        return S5_ERR_INVALID_ARGUMENT;
+    const size_t need = s5_bidirectional_workspace_size(B, L, H, P, u_dtype, y_dtype);
+    if (need == 0 || (size_t)B * L * H >= (1ull << 31)) return S5_ERR_UNSUPPORTED;
+    if (workspace_bytes < need) return S5_ERR_INVALID_ARGUMENT;
+    const BidiLayout l = bidi_layout(B, L, H, P, u_dtype, y_dtype);
+    char *w = static_cast<char *>(workspace);
+    float2 *cf = reinterpret_cast<float2 *>(w + l.cf), *cb = reinterpret_cast<float2 *>(w + l.cb);
+    float *d0 = reinterpret_cast<float *>(w + l.d0);
+    cudaError_t e = s5::launch_split_c(reinterpret_cast<const float2 *>(c_tilde2), H, P, cf, cb, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d0, 0, sizeof(float) * (size_t)H, st);
+    if (e == cudaSuccess)
+        e = s5::launch_reverse_time(u, w + l.ur, B, L, H, u_dtype == S5_BF16 ? 2 : 4, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    s5_status s = s5_forward(lambda_bar, b_bar, reinterpret_cast<const float *>(cf), d, u, u_dtype, y, y_dtype,
+                             proj_dtype, B, L, H, P, nullptr, nullptr, w, l.fwd, stream);
+    if (s != S5_OK) return s;
+    s = s5_forward(lambda_bar, b_bar, reinterpret_cast<const float *>(cb), d0, w + l.ur, u_dtype, w + l.yr, y_dtype,
+                   proj_dtype, B, L, H, P, nullptr, nullptr, w, l.fwd, stream);
+    if (s != S5_OK) return s;
+    e = s5::launch_add_reversed(y, w + l.yr, B, L, H, y_dtype == S5_BF16, st);
+    return e == cudaSuccess ? S5_OK : cuda_fail(e);
 }
 
 s5_status s5_sync_status(void *workspace, s5_stream_t stream) {

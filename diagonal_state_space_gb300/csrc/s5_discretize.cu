@@ -36,17 +36,40 @@ __device__ inline dcplx ddiv(dcplx a, dcplx b) {
 // (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z))/lambda;
 // below |z| = 1e-4, Delta * phi1(z) from its Taylor series.  Every thread of
 // the block then scales a slice of the B_tilde row.  Blocks have >= 128 threads.
+//
+// Options (all in float64, applied before the factors above):
+//   clip_re != 0   clip_eigs: Re(lambda) <- min(Re(lambda), clip_re)
+//                  (wikillm "Paper vs code": the official value is -1e-4);
+//   dt_scale       sampling-rate rescaling, Delta <- Delta * dt_scale with
+//                  dt_scale = old rate / new rate (review "Sampling intervals
+//                  carry physical meaning"; summary section 6.2);
+//   method 1       bilinear transform instead of the zero-order hold (review
+//                  "Discretization controls both retention and input gain";
+//                  the S4 page, "Discretize"): for a diagonal mode
+//                  lambda_bar = (1 + Delta lambda/2) / (1 - Delta lambda/2) and
+//                  gain = Delta / (1 - Delta lambda/2).
 __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float *__restrict__ log_dt,
                                   const float2 *__restrict__ b_tilde, int P, int H,
-                                  float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar) {
+                                  float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar, int method,
+                                  double clip_re, double dt_scale) {
     const int p = blockIdx.x;
     __shared__ double s_f[5];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2)
     __shared__ double s_gain[2];
     const float2 l = lambda[p];
-    const dcplx lam = {(double)l.x, (double)l.y};
-    const double dt = exp((double)log_dt[p]);
+    dcplx lam = {(double)l.x, (double)l.y};
+    if (clip_re != 0.0 && lam.re > clip_re) lam.re = clip_re;
+    const double dt = exp((double)log_dt[p]) * dt_scale;
     const dcplx z = {lam.re * dt, lam.im * dt};
-    if ((threadIdx.x & 31) == 0) {
+    if (method == 1) {
+        if (threadIdx.x == 0) {
+            const dcplx den = {1.0 - 0.5 * z.re, -0.5 * z.im};
+            const dcplx lb = ddiv(dcplx{1.0 + 0.5 * z.re, 0.5 * z.im}, den);
+            const dcplx gain = ddiv(dcplx{dt, 0.0}, den);
+            lambda_bar[p] = make_float2((float)lb.re, (float)lb.im);
+            s_gain[0] = gain.re;
+            s_gain[1] = gain.im;
+        }
+    } else if ((threadIdx.x & 31) == 0) {
         const int w = threadIdx.x >> 5;
         if (w == 0) sincos(z.im, &s_f[0], &s_f[1]);
         else if (w == 1) s_f[2] = exp(z.re);
@@ -54,7 +77,7 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
         else if (w == 3) s_f[4] = sin(0.5 * z.im);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (method != 1 && threadIdx.x == 0) {
         const double s = s_f[0], c = s_f[1], mag = s_f[2], em1r = s_f[3], sh = s_f[4];
         dcplx gain;
         const double zabs = sqrt(z.re * z.re + z.im * z.im);
@@ -112,9 +135,11 @@ __global__ void mode_consts_kernel(const float2 *__restrict__ lambda, const floa
 }
 
 cudaError_t launch_discretize(const float2 *lambda, const float *log_dt, const float2 *b_tilde,
-                              int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st) {
+                              int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st, int method,
+                              double clip_re, double dt_scale) {
     const int threads = H >= 256 ? 256 : 128;   // at least four warps (see discretize_kernel)
-    discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar);
+    discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar, method, clip_re,
+                                             dt_scale);
     return cudaGetLastError();
 }
 

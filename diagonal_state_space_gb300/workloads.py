@@ -52,6 +52,7 @@ class Workload:
     u_dtype: str = "f32"      # storage type of u and y: "f32" or "bf16"
     proj_dtype: str = "f32"   # input type of the two projections
     varying_dt: bool = False  # per-step interval g_k * Delta_n
+    bidirectional: bool = False  # forward and backward scans, C~ [H, 2P]
     layers: int = 0           # > 0: layer stack (pre-LN, SSM, gate, residual)
     seed: int = 0
     notes: str = field(default="", compare=False)
@@ -72,6 +73,9 @@ WORKLOADS = {
     "pathx_bf16": Workload("pathx_bf16", 8, 16384, 128, 128, u_dtype="bf16",
                            proj_dtype="bf16", seed=2000,
                            notes="long sequence, bf16 u/y and projections, complex fp32 scan"),
+    "pathx_bf16_bidir": Workload("pathx_bf16_bidir", 8, 16384, 128, 128, u_dtype="bf16",
+                                 proj_dtype="bf16", bidirectional=True, seed=2000,
+                                 notes="the long-sequence shapes through the bidirectional layer"),
     "irregular": Workload("irregular", 32, 2048, 256, 128, varying_dt=True, seed=3000,
                           notes="per-step interval g_k*Delta_n, fp32"),
     "stack6": Workload("stack6", 32, 1024, 512, 256, u_dtype="f32", proj_dtype="bf16",
@@ -104,7 +108,7 @@ def layer_params(rng, H: int, P: int) -> dict:
 
 
 def make_layer_inputs(B: int, L: int, H: int, P: int, seed: int, u_dtype: str = "f32",
-                      varying_dt: bool = False) -> dict:
+                      varying_dt: bool = False, bidirectional: bool = False) -> dict:
     """Inputs of one S5 layer.  Keys: u (float32 values; bf16-representable when
     u_dtype == "bf16"), lambda_ (complex64 [P]), log_dt, b_tilde, c_tilde, d and,
     for irregular sampling, g [B, L]."""
@@ -116,6 +120,13 @@ def make_layer_inputs(B: int, L: int, H: int, P: int, seed: int, u_dtype: str = 
     out.update(layer_params(rng, H, P))
     if varying_dt:
         out["g"] = rng.exponential(1.0, (B, L)).astype(np.float32)
+    if bidirectional:
+        # C~ of the backward modes: the same complex-normal generator, its own stream
+        rb = np.random.Generator(np.random.PCG64(seed + 1))
+        sc = np.float32(np.sqrt(1.0 / (2 * H)))
+        cb = (rb.standard_normal((H, P), dtype=np.float32) * sc
+              + 1j * rb.standard_normal((H, P), dtype=np.float32) * sc).astype(np.complex64)
+        out["c_tilde2"] = np.ascontiguousarray(np.concatenate([out["c_tilde"], cb], axis=1))
     return out
 
 
@@ -140,4 +151,4 @@ def make_inputs(w: Workload, B: int | None = None) -> dict:
     Bn = w.B if B is None else B
     if w.layers:
         return make_stack_inputs(Bn, w.L, w.H, w.P, w.layers, w.seed)
-    return make_layer_inputs(Bn, w.L, w.H, w.P, w.seed, w.u_dtype, w.varying_dt)
+    return make_layer_inputs(Bn, w.L, w.H, w.P, w.seed, w.u_dtype, w.varying_dt, w.bidirectional)

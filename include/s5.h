@@ -50,6 +50,8 @@ typedef enum {
 
 typedef enum { S5_F32 = 0, S5_BF16 = 1 } s5_dtype;
 
+typedef enum { S5_ZOH = 0, S5_BILINEAR = 1 } s5_discretization;
+
 /*
  * Zero-order-hold discretisation ("SIMPLIFIED STATE SPACE LAYERS ...",
  * section 3.2 eq. 6; review row 2):
@@ -67,6 +69,30 @@ typedef enum { S5_F32 = 0, S5_BF16 = 1 } s5_dtype;
  */
 s5_status s5_discretize(const float *lambda, const float *log_dt, const float *b_tilde,
                         int P, int H, float *lambda_bar, float *b_bar, s5_stream_t stream);
+
+/*
+ * Discretisation with the options of the official implementation.
+ *   method  S5_ZOH as s5_discretize, or S5_BILINEAR (review "Discretization
+ *           controls both retention and input gain": the official code offers
+ *           the bilinear transform beside ZOH; the S4 page, "Discretize",
+ *           prints it): per mode
+ *             lambda_bar_n = (1 + Delta_n lambda_n / 2) / (1 - Delta_n lambda_n / 2)
+ *             b_bar[n,:]   = Delta_n / (1 - Delta_n lambda_n / 2) * b_tilde[n,:]
+ *   clip_re clip_eigs ("Simplified State Space Layers ...", "Paper vs code":
+ *           the real part of lambda clipped to at most -1e-4): when non-zero,
+ *           Re(lambda_n) is replaced by min(Re(lambda_n), clip_re) before
+ *           discretising.  0 disables clipping; a positive value is rejected.
+ *   dt_scale sampling-rate rescaling (review "Sampling intervals carry
+ *           physical meaning"; summary section 6.2):
+ *           Delta_n = dt_scale * exp(log_dt[n]) with dt_scale = old sampling
+ *           rate / new sampling rate (16 kHz -> 8 kHz gives 2).  Must be > 0.
+ * Computed in float64 on the device and rounded once.  Arrays as in
+ * s5_discretize.  Errors: S5_ERR_INVALID_ARGUMENT for null/misaligned
+ * pointers, P, H < 1, an unknown method, dt_scale <= 0 or clip_re > 0.
+ */
+s5_status s5_discretize_ex(const float *lambda, const float *log_dt, const float *b_tilde, int P, int H,
+                           s5_discretization method, float clip_re, float dt_scale, float *lambda_bar,
+                           float *b_bar, s5_stream_t stream);
 
 /*
  * Forward pass of the time-invariant layer over B sequences of length L
@@ -112,6 +138,47 @@ s5_status s5_forward_varying_dt(const float *lambda, const float *log_dt, const 
                                 s5_dtype proj_dtype, int B, int L, int H, int P,
                                 const float *x0, float *x_last, void *workspace,
                                 size_t workspace_bytes, s5_stream_t stream);
+
+/*
+ * One streaming step of B independent sequences (review "Associative scans
+ * preserve the recurrence": streaming inference keeps just the current state;
+ * summary App. C.1, online generation at O(PH) per step):
+ *   x_b <- lambda_bar * x_b + b_bar u_b
+ *   y_b  = 2 Re(c_tilde x_b) + d * u_b
+ *   lambda_bar [P], b_bar [P,H], c_tilde [H,P] complex; d [H] float32
+ *   x [B,P] complex, updated in place (the state of s5_forward's x0 / x_last)
+ *   u [B,H] float32 in; y [B,H] float32 out
+ * Float32 throughout.  Errors: S5_ERR_INVALID_ARGUMENT for null/misaligned
+ * pointers or B < 0, H < 1, P < 1; B = 0 is a no-op (x, u, y may then be
+ * null); S5_ERR_UNSUPPORTED when 8P + 4H bytes of state and input exceed 48 KiB.
+ */
+s5_status s5_step(const float *lambda_bar, const float *b_bar, const float *c_tilde, const float *d,
+                  float *x, const float *u, float *y, int B, int H, int P, s5_stream_t stream);
+
+/*
+ * Bidirectional layer ("Simplified State Space Layers ...", "Paper vs code":
+ * the code runs a forward and a backward scan and concatenates them, so C~
+ * has 2P columns; review "Published results": the backward scan sees future
+ * inputs, so this is for offline use).  Both scans use lambda_bar and b_bar:
+ *   xf_k = lambda_bar * xf_{k-1} + b_bar u_k,   xf_0 = 0
+ *   xb_k = lambda_bar * xb_{k+1} + b_bar u_k,   xb_{L+1} = 0
+ *   y_k  = 2 Re(c_tilde2[:, 0:P] xf_k + c_tilde2[:, P:2P] xb_k) + d * u_k
+ *   c_tilde2 [H,2P] complex; other arrays, dtypes and proj_dtype as in
+ *   s5_forward (the same kernel path is chosen for both scans).
+ *   workspace: at least s5_bidirectional_workspace_size(B,L,H,P,u_dtype,y_dtype)
+ *   bytes, zero-filled before its first use.
+ * Runs as: the two halves of c_tilde2 split into [H,P] arrays, u reversed in
+ * time, s5_forward on u (with d) and on the reversed u (with d = 0), and the
+ * second result reversed and added into y -- all on `stream`.
+ * Errors: those of s5_forward; S5_ERR_UNSUPPORTED when B*L*H >= 2^31.
+ */
+s5_status s5_forward_bidirectional(const float *lambda_bar, const float *b_bar, const float *c_tilde2,
+                                   const float *d, const void *u, s5_dtype u_dtype, void *y,
+                                   s5_dtype y_dtype, s5_dtype proj_dtype, int B, int L, int H, int P,
+                                   void *workspace, size_t workspace_bytes, s5_stream_t stream);
+
+/* Bytes of workspace s5_forward_bidirectional needs; 0 for invalid sizes. */
+size_t s5_bidirectional_workspace_size(int B, int L, int H, int P, s5_dtype u_dtype, s5_dtype y_dtype);
 
 /* Bytes of workspace that s5_forward / s5_forward_varying_dt need for these
  * sizes (carry flags and per-tile aggregates of the chunked scan, plus a

@@ -76,6 +76,45 @@ def discretize(lam, log_dt, b_tilde):
     return lb, bb
 
 
+def discretize_ex(lam, log_dt, b_tilde, method="zoh", clip_re=0.0, dt_scale=1.0):
+    """Discretisation with options: method "zoh" or "bilinear", clip_eigs
+    threshold clip_re (0 = none; the official value is -1e-4), and the
+    sampling-rate rescaling factor dt_scale = old rate / new rate."""
+    lam, log_dt, b_tilde = _c128(lam), _f64(log_dt), _c128(b_tilde)
+    P, H = b_tilde.shape
+    lb = np.empty(P, np.complex128)
+    bb = np.empty((P, H), np.complex128)
+    m = {"zoh": 0, "bilinear": 1}[method]
+    _load().s5o_discretize_ex(_I(P), _I(H), _p(lam), _p(log_dt), _p(b_tilde), _I(m),
+                              ctypes.c_double(clip_re), ctypes.c_double(dt_scale), _p(lb), _p(bb))
+    return lb, bb
+
+
+def step(lambda_bar, b_bar, c_tilde, d, x, u):
+    """One streaming step: returns (x_new [B,P], y [B,H]) for x [B,P], u [B,H]."""
+    lb, bb, ct, d = _c128(lambda_bar), _c128(b_bar), _c128(c_tilde), _f64(d)
+    x = _c128(x).copy()
+    u = _f64(u)
+    Bn, H = u.shape
+    P = lb.shape[0]
+    y = np.empty((Bn, H), np.float64)
+    _load().s5o_step(_I(Bn), _I(H), _I(P), _p(lb), _p(bb), _p(ct), _p(d), _p(x), _p(u), _p(y))
+    return x, y
+
+
+def forward_bidirectional(lambda_bar, b_bar, c_tilde2, d, u):
+    """Bidirectional layer over u [B,L,H] with C~ [H,2P] (forward modes, then
+    backward modes); returns y [B,L,H]."""
+    lb, bb, ct, d, u = _c128(lambda_bar), _c128(b_bar), _c128(c_tilde2), _f64(d), _f64(u)
+    Bn, L, H = u.shape
+    P = lb.shape[0]
+    assert ct.shape == (H, 2 * P)
+    y = np.empty((Bn, L, H), np.float64)
+    _load().s5o_forward_bidirectional(_I(Bn), _I(L), _I(H), _I(P), _p(lb), _p(bb), _p(ct), _p(d),
+                                      _p(u), _p(y))
+    return y
+
+
 def forward(lambda_bar, b_bar, c_tilde, d, u, x0=None, return_states=False):
     """Time-invariant layer over u [B,L,H]; returns y [B,L,H] and x_last [B,P]
     (or all states [B,L,P] when ``return_states``)."""

@@ -86,6 +86,46 @@ void s5o_discretize(int P, int H, const cplx *lambda, const double *log_dt,
 /* is a regrouping of exactly this loop.  [S5-review] row 4 and [S5-wiki]    */
 /* "Paper vs code": y_k = 2 Re(C-tilde x_k) + D*u_k, D not doubled.          */
 /* ------------------------------------------------------------------------ */
+/* Discretisation options.                                                   */
+/*                                                                           */
+/* Bilinear transform ([S5-review] "Discretization controls both retention   */
+/* and input gain": the official code offers it beside ZOH; the S4 page,     */
+/* section 2.3 "Discretize", prints it for a general A): with               */
+/* A-bar = (I - dt/2 A)^-1 (I + dt/2 A) and B-bar = (I - dt/2 A)^-1 dt B, a  */
+/* diagonal A gives per mode                                                 */
+/*     lambda-bar = (1 + dt lambda / 2) / (1 - dt lambda / 2),               */
+/*     gain       = dt / (1 - dt lambda / 2).                                */
+/* clip_eigs ([S5-wiki] "Paper vs code"): Re(lambda) is clipped to at most   */
+/* clip_re before discretising (the official value is -1e-4; clip_re = 0     */
+/* means no clipping).  Sampling-rate rescaling ([S5-review] "Sampling       */
+/* intervals carry physical meaning"; [S5-notes] section 6.2): dt is         */
+/* multiplied by dt_scale = old rate / new rate.                             */
+/* method 0 = zero-order hold, 1 = bilinear.                                 */
+/* ------------------------------------------------------------------------ */
+void s5o_discretize_ex(int P, int H, const cplx *lambda, const double *log_dt,
+                       const cplx *b_tilde, int method, double clip_re,
+                       double dt_scale, cplx *lambda_bar, cplx *b_bar)
+{
+    for (int p = 0; p < P; ++p) {
+        cplx lam = lambda[p];
+        if (clip_re != 0.0 && creal(lam) > clip_re)
+            lam = clip_re + I * cimag(lam);
+        double dt = exp(log_dt[p]) * dt_scale;
+        cplx gain;
+        if (method == 1) {
+            cplx den = 1.0 - 0.5 * dt * lam;
+            lambda_bar[p] = (1.0 + 0.5 * dt * lam) / den;
+            gain = dt / den;
+        } else {
+            lambda_bar[p] = cexp(lam * dt);
+            gain = zoh_gain(lam, dt);
+        }
+        for (int h = 0; h < H; ++h)
+            b_bar[(size_t)p * H + h] = gain * b_tilde[(size_t)p * H + h];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 static void forward_one(int L, int H, int P, const cplx *lambda_bar,
                         const cplx *b_bar, const cplx *c_tilde, const double *d,
                         const double *u, cplx *x, double *y, cplx *states)
@@ -429,4 +469,70 @@ void s5o_stack(int nl, int B, int L, int H, int P,
         free(ubar); free(ybar); free(zbar); free(s); free(xhat); free(gbbar); free(glbar);
     }
     free(us); free(zs); free(ys); free(xs); free(lbar); free(bbar); free(hid); free(act);
+}
+
+/* ------------------------------------------------------------------------ */
+/* One streaming step ([S5-review] "Associative scans preserve the           */
+/* recurrence": streaming inference keeps just the current state per layer;  */
+/* [S5-notes] App. C.1, online generation): per sequence b,                  */
+/*     x <- lambda-bar * x + B-bar u,   y = 2 Re(C-tilde x) + D * u.         */
+/* x [B,P] is updated in place; u, y [B,H].                                  */
+/* ------------------------------------------------------------------------ */
+void s5o_step(int B, int H, int P, const cplx *lambda_bar, const cplx *b_bar,
+              const cplx *c_tilde, const double *d, cplx *x, const double *u,
+              double *y)
+{
+    for (int b = 0; b < B; ++b)
+        forward_one(1, H, P, lambda_bar, b_bar, c_tilde, d, u + (size_t)b * H,
+                    x + (size_t)b * P, y + (size_t)b * H, NULL);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bidirectional layer ([S5-wiki] "Paper vs code": the code runs a forward   */
+/* and a backward scan and concatenates them, so C-tilde has 2P columns;     */
+/* [S5-review] "Published results": a backward scan sees future inputs).     */
+/* Reading: both scans use the same lambda-bar and B-bar; the backward one   */
+/*     xb_k = lambda-bar * xb_{k+1} + B-bar u_k,   xb_{L+1} = 0,             */
+/* and y_k = 2 Re(C-tilde [xf_k ; xb_k]) + D * u_k, C-tilde [H, 2P] with the */
+/* forward modes in columns 0..P-1 and the backward ones in P..2P-1.          */
+/* ------------------------------------------------------------------------ */
+void s5o_forward_bidirectional(int B, int L, int H, int P, const cplx *lambda_bar,
+                               const cplx *b_bar, const cplx *c_tilde2,
+                               const double *d, const double *u, double *y)
+{
+    cplx *xf = malloc(sizeof(cplx) * (size_t)L * P);
+    cplx *xb = malloc(sizeof(cplx) * (size_t)L * P);
+    cplx *x = malloc(sizeof(cplx) * (size_t)P);
+    for (int b = 0; b < B; ++b) {
+        const double *ub = u + (size_t)b * L * H;
+        for (int p = 0; p < P; ++p) x[p] = 0.0;
+        for (int k = 0; k < L; ++k)
+            for (int p = 0; p < P; ++p) {
+                cplx bu = 0.0;
+                for (int h = 0; h < H; ++h)
+                    bu += b_bar[(size_t)p * H + h] * ub[(size_t)k * H + h];
+                x[p] = lambda_bar[p] * x[p] + bu;
+                xf[(size_t)k * P + p] = x[p];
+            }
+        for (int p = 0; p < P; ++p) x[p] = 0.0;
+        for (int k = L - 1; k >= 0; --k)
+            for (int p = 0; p < P; ++p) {
+                cplx bu = 0.0;
+                for (int h = 0; h < H; ++h)
+                    bu += b_bar[(size_t)p * H + h] * ub[(size_t)k * H + h];
+                x[p] = lambda_bar[p] * x[p] + bu;
+                xb[(size_t)k * P + p] = x[p];
+            }
+        for (int k = 0; k < L; ++k)
+            for (int h = 0; h < H; ++h) {
+                cplx cx = 0.0;
+                for (int p = 0; p < P; ++p)
+                    cx += c_tilde2[(size_t)h * 2 * P + p] * xf[(size_t)k * P + p] +
+                          c_tilde2[(size_t)h * 2 * P + P + p] * xb[(size_t)k * P + p];
+                y[((size_t)b * L + k) * H + h] = 2.0 * creal(cx) + d[h] * ub[(size_t)k * H + h];
+            }
+    }
+    free(xf);
+    free(xb);
+    free(x);
 }

@@ -1,0 +1,180 @@
+"""GPU parity of the options and variants beyond the causal layer: the
+discretisation options (bilinear, clip_eigs, rate rescaling), the streaming
+step, the bidirectional layer, and a forward pass from the HiPPO-N
+initialiser.  CUDA path through the C ABI against the float64 oracle on the
+same seeded inputs.
+
+Bars: discretisation is float64 on the device rounded once (2e-7 relative per
+element); float32 paths 1e-5 relative L2 per output tensor; bf16 paths 2e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diagonal_state_space_gb300 import api
+from diagonal_state_space_gb300 import init as s5init
+from diagonal_state_space_gb300._native import S5Error
+from diagonal_state_space_gb300.workloads import bf16_round, make_layer_inputs
+
+from _parity import dev, host, layer_to_device, rel_l2
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = 1e-5
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    torch.cuda.init()
+
+
+# --------------------------------------------------------------------------
+# discretisation options
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("method", ["zoh", "bilinear"])
+@pytest.mark.parametrize("clip_re,dt_scale", [(0.0, 1.0), (-1e-4, 1.0), (0.0, 2.0), (-1e-4, 0.5)])
+@pytest.mark.parametrize("P,H", [(1, 1), (64, 128), (300, 7)])
+def test_discretize_ex_matches_oracle(method, clip_re, dt_scale, P, H):
+    inp = make_layer_inputs(1, 1, H, P, seed=11 + P + H)
+    lam = inp["lambda_"].copy()
+    lam[::3] = (np.abs(lam[::3].real) * 0.5 + 1j * lam[::3].imag).astype(np.complex64)  # some Re > 0: clipped
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize_ex(dev(lam), t["log_dt"], t["b_tilde"], method, clip_re, dt_scale)
+    olb, obb = oracle.discretize_ex(lam, inp["log_dt"], inp["b_tilde"], method, clip_re,
+                                    float(np.float32(dt_scale)))
+    np.testing.assert_allclose(host(lb), olb, rtol=2e-7, atol=1e-30)
+    np.testing.assert_allclose(host(bb), obb, rtol=3e-7, atol=1e-12 * np.max(np.abs(obb)))
+
+
+def test_discretize_ex_zoh_equals_discretize():
+    inp = make_layer_inputs(1, 1, 48, 40, seed=3)
+    t = layer_to_device(inp)
+    a = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    b = api.s5_discretize_ex(t["lam"], t["log_dt"], t["b_tilde"])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_discretize_ex_rejects_bad_options():
+    inp = make_layer_inputs(1, 1, 8, 4, seed=3)
+    t = layer_to_device(inp)
+    for kw in (dict(dt_scale=0.0), dict(dt_scale=-1.0), dict(clip_re=1e-3)):
+        with pytest.raises(S5Error):
+            api.s5_discretize_ex(t["lam"], t["log_dt"], t["b_tilde"], **kw)
+
+
+# --------------------------------------------------------------------------
+# streaming step
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("B,H,P,steps", [(1, 1, 1, 3), (3, 32, 16, 20), (8, 128, 128, 8), (2, 300, 70, 5)])
+def test_step_matches_oracle(B, H, P, steps):
+    inp = make_layer_inputs(B, steps, H, P, seed=21 + H)
+    olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    rng = np.random.default_rng(5)
+    x0 = (rng.standard_normal((B, P)) + 1j * rng.standard_normal((B, P))).astype(np.complex64)
+    x = dev(x0)
+    ox = x0.astype(np.complex128)
+    for k in range(steps):
+        uk = np.ascontiguousarray(inp["u"][:, k])
+        y = api.s5_step(lb, bb, t["c_tilde"], t["d"], x, dev(uk))
+        ox, oy = oracle.step(host(lb), host(bb), inp["c_tilde"], inp["d"], ox, uk)
+        assert rel_l2(host(y), oy) <= FP32_TOL
+        # the D*u-free part alone
+        assert rel_l2(host(y) - inp["d"] * uk, oy - inp["d"] * uk) <= FP32_TOL
+    assert rel_l2(host(x), ox) <= FP32_TOL
+
+
+def test_steps_continue_a_forward_pass():
+    B, L, H, P = 2, 37, 32, 16
+    inp = make_layer_inputs(B, L + 4, H, P, seed=9)
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    y_all = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"])
+    _, xl = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"][:, :L].contiguous(), x_last=True)
+    for k in range(L, L + 4):
+        yk = api.s5_step(lb, bb, t["c_tilde"], t["d"], xl, t["u"][:, k].contiguous())
+        assert rel_l2(host(yk), host(y_all[:, k])) <= FP32_TOL
+
+
+def test_step_rejects_misaligned_and_empty_batch_is_a_noop():
+    inp = make_layer_inputs(2, 1, 8, 4, seed=3)
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    x = torch.zeros(2, 4, dtype=torch.complex64, device="cuda")
+    u = torch.zeros(2 * 8 + 1, dtype=torch.float32, device="cuda")[1:].view(2, 8)
+    with pytest.raises(S5Error):
+        api.s5_step(lb, bb, t["c_tilde"], t["d"], x, u)
+    x0 = torch.zeros(0, 4, dtype=torch.complex64, device="cuda")
+    y0 = api.s5_step(lb, bb, t["c_tilde"], t["d"], x0, torch.zeros(0, 8, device="cuda"))
+    assert y0.shape == (0, 8)
+
+
+# --------------------------------------------------------------------------
+# bidirectional layer
+# --------------------------------------------------------------------------
+def _c2(inp, seed):
+    rng = np.random.default_rng(seed)
+    H, P = inp["c_tilde"].shape
+    cb = ((rng.standard_normal((H, P)) + 1j * rng.standard_normal((H, P))) / np.sqrt(2 * H)).astype(np.complex64)
+    return np.ascontiguousarray(np.concatenate([inp["c_tilde"], cb], axis=1))
+
+
+@pytest.mark.parametrize("B,L,H,P", [(1, 1, 8, 4), (2, 77, 32, 16), (3, 300, 64, 24), (1, 1000, 128, 64)])
+def test_bidirectional_f32_matches_oracle(B, L, H, P):
+    inp = make_layer_inputs(B, L, H, P, seed=31 + L)
+    c2 = _c2(inp, L)
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    for dz in (False, True):
+        d = np.zeros_like(inp["d"]) if dz else inp["d"]
+        y = api.s5_forward_bidirectional(lb, bb, dev(c2), dev(d), t["u"])
+        oy = oracle.forward_bidirectional(host(lb), host(bb), c2, d, inp["u"])
+        assert rel_l2(host(y), oy) <= FP32_TOL, (dz, rel_l2(host(y), oy))
+
+
+@pytest.mark.parametrize("B,L", [(2, 700), (1, 4096)])
+def test_bidirectional_bf16_tensor_core_path_matches_oracle(B, L):
+    H = P = 128
+    inp = make_layer_inputs(B, L, H, P, seed=41 + L, u_dtype="bf16")
+    c2 = _c2(inp, L)
+    t = layer_to_device(inp, "bf16")
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    y = api.s5_forward_bidirectional(lb, bb, dev(c2), t["d"], t["u"], proj_dtype="bf16")
+    assert y.dtype == torch.bfloat16
+    oy = oracle.forward_bidirectional(host(lb), host(bb), c2, inp["d"], inp["u"])
+    assert rel_l2(host(y.float()), oy) <= BF16_TOL
+    # the SSM terms alone (D = 0)
+    y0 = api.s5_forward_bidirectional(lb, bb, dev(c2), dev(np.zeros(H, np.float32)), t["u"], proj_dtype="bf16")
+    oy0 = oracle.forward_bidirectional(host(lb), host(bb), c2, np.zeros(H), inp["u"])
+    assert rel_l2(host(y0.float()), oy0) <= BF16_TOL
+
+
+def test_bidirectional_with_zero_backward_half_is_the_causal_layer():
+    B, L, H, P = 2, 200, 32, 16
+    inp = make_layer_inputs(B, L, H, P, seed=5)
+    c2 = np.ascontiguousarray(np.concatenate([inp["c_tilde"], np.zeros_like(inp["c_tilde"])], axis=1))
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    yb = api.s5_forward_bidirectional(lb, bb, dev(c2), t["d"], t["u"])
+    yf = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"])
+    assert rel_l2(host(yb), host(yf)) <= 1e-6
+
+
+# --------------------------------------------------------------------------
+# HiPPO-N initialisation through the layer
+# --------------------------------------------------------------------------
+def test_forward_from_hippo_init_matches_oracle():
+    B, L, H, P = 2, 300, 32, 16
+    lam, log_dt, bt, ct, d = s5init.init_s5(P, H, blocks=2, seed=7)
+    rng = np.random.default_rng(7)
+    u = rng.standard_normal((B, L, H)).astype(np.float32)
+    lb, bb = api.s5_discretize(dev(lam), dev(log_dt), dev(bt))
+    y = api.s5_forward(lb, bb, dev(ct), dev(d), dev(u))
+    olb, obb = oracle.discretize(lam, log_dt, bt)
+    oy, _ = oracle.forward(olb, obb, ct, d, u)
+    assert rel_l2(host(y), oy) <= FP32_TOL
