@@ -32,20 +32,32 @@ sys.path.insert(0, ROOT)
 
 METRIC = "S5 layer fwd tokens/s (batch*L/s) and fraction of HBM/tensor roofline"
 BIDI_METRIC = "S5 bidirectional layer fwd tokens/s (batch*L/s) and fraction of HBM/tensor roofline"
+STREAM_METRIC = "S5 streaming step tokens/s (batch tokens per step call / call time)"
 FALLBACK_HBM_GBS = 6800.0
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000; 20 for the streaming workload, whose step "
+                         "is 1024 calls)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default 50; 3 for stream)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="pathx_bf16",
-                    choices=["small", "fp32", "pathx_bf16", "pathx_bf16_bidir", "irregular", "stack6"])
-    ap.add_argument("--e2e-steps", type=int, default=30)
+                    choices=["small", "fp32", "pathx_bf16", "pathx_bf16_bidir", "pathx_bf16_bilinear",
+                             "stream", "irregular", "stack6"])
+    ap.add_argument("--e2e-steps", type=int, default=None, help="end-to-end steps (default 30; 3 for stream)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    args = ap.parse_args()
+    stream = args.workload == "stream"
+    if args.steps is None:
+        args.steps = 20 if stream else 2000
+    if args.warmup is None:
+        args.warmup = 3 if stream else 50
+    if args.e2e_steps is None:
+        args.e2e_steps = 3 if stream else 30
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -152,6 +164,14 @@ def algorithmic_bytes(w, u_bytes_per, y_bytes_per):
     return w.B * w.L * w.H * (u_bytes_per + y_bytes_per) + params
 
 
+def graph_event(torch):
+    """A timing event that can be recorded inside a CUDA graph capture."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:      # torch without external events: plain timing events
+        return torch.cuda.Event(enable_timing=True)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -189,16 +209,18 @@ def run_ours(args):
                and not w.varying_dt)
     fwd_ev = []
 
-    def new_event():
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:      # torch without external events: plain timing events
-            return torch.cuda.Event(enable_timing=True)
+    new_event = lambda: graph_event(torch)
+
+    def discretize(lam_, log_dt_, bt_):
+        if w.method == "zoh" and w.clip_re == 0.0 and w.dt_scale == 1.0:
+            return api.s5_discretize(lam_, log_dt_, bt_, lb, bb)
+        return api.s5_discretize_ex(lam_, log_dt_, bt_, method=w.method, clip_re=w.clip_re,
+                                    dt_scale=w.dt_scale, lambda_bar=lb, b_bar=bb)
 
     def step(i, timed):
         u, y = u_sets[i % NSETS], y_sets[i % NSETS]
         if not w.varying_dt:
-            api.s5_discretize(lam, log_dt, bt, lb, bb)
+            discretize(lam, log_dt, bt)
         if timed:
             e0, e1 = new_event(), new_event()
             e0.record()
@@ -287,7 +309,7 @@ def run_ours(args):
             api.s5_forward_varying_dt(*dev_params[:5], dev_params[5], u_dev, y=y_dev,
                                       proj_dtype=w.proj_dtype, workspace=ws)
         else:
-            l_, b_ = api.s5_discretize(dev_params[0], dev_params[1], dev_params[2], lb, bb)
+            l_, b_ = discretize(dev_params[0], dev_params[1], dev_params[2])
             if w.bidirectional:
                 api.s5_forward_bidirectional(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
                                              proj_dtype=w.proj_dtype, workspace=ws)
@@ -357,7 +379,10 @@ def run_ours(args):
             "global_batch": w.B * world, "seq_len": w.L, "H": w.H, "P": w.P,
             "step": ("s5_forward_varying_dt" if w.varying_dt else
                      "s5_discretize + s5_forward_bidirectional" if w.bidirectional else
-                     "s5_discretize + s5_forward"),
+                     "s5_discretize + s5_forward" if w.method == "zoh" and w.clip_re == 0.0
+                     and w.dt_scale == 1.0 else
+                     "s5_discretize_ex(%s, clip_re=%g, dt_scale=%g) + s5_forward" % (
+                         w.method, w.clip_re, w.dt_scale)),
             "arithmetic": ("bf16 tensor-core projections (fp32 accumulate), complex fp32 scan"
                            if tc_path else "fp32 CUDA-core projections, complex fp32 scan"),
             "timing": "K steps captured in one CUDA graph, replayed once between events",
@@ -385,6 +410,152 @@ def run_ours(args):
         # or, with per-step intervals, mode constants + CUDA-core forward
         # bidirectional: discretize, split, reverse, 2 x (images + forward | forward), add
         "gpu_launches": args.steps * ((8 if tc_path else 6) if w.bidirectional else (3 if tc_path else 2)),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def run_stream(args):
+    """Streaming inference through s5_step: one bench step feeds L tokens to
+    each of the B sequences, one s5_step call per token."""
+    import numpy as np
+    import torch
+
+    from diagonal_state_space_gb300 import api
+    from diagonal_state_space_gb300.workloads import WORKLOADS, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    lam, log_dt, bt, ct, d = (dev(inp[k]) for k in ("lambda_", "log_dt", "b_tilde", "c_tilde", "d"))
+    # time-major [L, B, H]: the k-th call reads and writes one contiguous [B, H] slice
+    u_t = dev(np.transpose(inp["u"], (1, 0, 2)))
+    y_t = torch.empty_like(u_t)
+    x = torch.zeros(w.B, w.P, dtype=torch.complex64, device="cuda")
+    lb, bb = api.s5_discretize(lam, log_dt, bt)
+    stream = torch.cuda.current_stream()
+    loop_ev = []
+
+    def step(timed):
+        api.s5_discretize(lam, log_dt, bt, lb, bb)
+        if timed:
+            e0, e1 = graph_event(torch), graph_event(torch)
+            e0.record()
+        for k in range(w.L):
+            api.s5_step(lb, bb, ct, d, x, u_t[k], y=y_t[k])
+        if timed:
+            e1.record()
+            loop_ev.append((e0, e1))
+
+    for _ in range(max(3, args.warmup)):
+        step(False)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step(True)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    call_s = statistics.fmean(a.elapsed_time(b) for a, b in loop_ev) / 1e3 / w.L
+    tokens = w.B * w.L
+    value = tokens * world / (ms_step / 1e3)
+
+    # end to end: host u in, host y out, every call through the public API
+    u_host = torch.from_numpy(np.ascontiguousarray(np.transpose(inp["u"], (1, 0, 2)))).pin_memory()
+    y_host = torch.empty_like(u_host).pin_memory()
+    host_params = [torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+                   for k in ("lambda_", "log_dt", "b_tilde", "c_tilde", "d")]
+    dev_params = [torch.empty_like(p, device="cuda") for p in host_params]
+
+    def e2e_step():
+        for hp, dp in zip(host_params, dev_params):
+            dp.copy_(hp, non_blocking=True)
+        u_t.copy_(u_host, non_blocking=True)
+        l_, b_ = api.s5_discretize(dev_params[0], dev_params[1], dev_params[2], lb, bb)
+        for k in range(w.L):
+            api.s5_step(l_, b_, dev_params[3], dev_params[4], x, u_t[k], y=y_t[k])
+        y_host.copy_(y_t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = u_host.numel() * 4 + sum(p.numel() * p.element_size() for p in host_params)
+    d2h = y_host.numel() * 4
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return None
+
+    hbm_gbs, _, peak_kind = load_peaks()
+    # per call: lambda_bar, B_bar, C~, D once; the state read and written; u and y
+    alg = 8 * w.P + 16 * w.P * w.H + 4 * w.H + 16 * w.B * w.P + 8 * w.B * w.H
+    achieved = alg / call_s / 1e9
+    result = {
+        "metric": STREAM_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64, the recipe of the layer workloads)",
+        "config": {
+            "workload": "%s: S5 streaming step, B=%d sequences x %d single-token s5_step calls, "
+                        "H=%d P=%d, fp32" % (w.name, w.B, w.L, w.H, w.P),
+            "global_batch": w.B * world, "seq_len": w.L, "H": w.H, "P": w.P,
+            "step": "s5_discretize + %d x s5_step" % w.L,
+            "timing": "K steps captured in one CUDA graph, replayed once between events",
+            "l2": "parameters (%.0f KB) stay L2-resident by design: the step reuses them every "
+                  "call" % (alg / 1e3),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "step_kernel", "achieved": achieved, "peak": hbm_gbs,
+            "unit": "GB/s", "frac": achieved / hbm_gbs,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                           if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": alg, "launch_us": call_s * 1e6, "traffic": None,
+            "note": "a dependent chain of small launches: bound by launch latency, not bandwidth",
+        },
+        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (1 + w.L),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -566,7 +737,15 @@ def oracle_run(w, inp, seqs):
     if w.varying_dt:
         return oracle.forward_varying_dt(inp["lambda_"], inp["log_dt"], inp["b_tilde"],
                                          inp["c_tilde"], inp["d"], inp["g"][seqs], inp["u"][seqs])
-    lb, bb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    lb, bb = oracle.discretize_ex(inp["lambda_"], inp["log_dt"], inp["b_tilde"], method=w.method,
+                                  clip_re=w.clip_re, dt_scale=w.dt_scale)
+    if w.streaming:
+        import numpy as np
+        x = np.zeros((len(seqs), w.P), np.complex128)
+        y = np.empty((len(seqs), w.L, w.H))
+        for k in range(w.L):
+            x, y[:, k] = oracle.step(lb, bb, inp["c_tilde"], inp["d"], x, inp["u"][seqs, k])
+        return y
     if w.bidirectional:
         return oracle.forward_bidirectional(lb, bb, inp["c_tilde2"], inp["d"], inp["u"][seqs])
     return oracle.forward(lb, bb, inp["c_tilde"], inp["d"], inp["u"][seqs])
@@ -604,7 +783,8 @@ def run_reference(args):
     dt = (time.perf_counter() - t0) / steps
     v = len(seqs) * w.L / dt
     sample = "%d sequence x %d tokens per step (of %d sequences)" % (len(seqs), w.L, w.B)
-    res = {"metric": BIDI_METRIC if w.bidirectional else METRIC, "value": v, "unit": "tokens/s",
+    res = {"metric": (BIDI_METRIC if w.bidirectional else STREAM_METRIC if w.streaming else METRIC),
+           "value": v, "unit": "tokens/s",
            "n_gpus": world, "steps": steps,
            "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
@@ -624,6 +804,8 @@ def main():
         run_reference(args)
     elif args.workload == "stack6":
         run_stack(args)
+    elif args.workload == "stream":
+        run_stream(args)
     else:
         run_ours(args)
 

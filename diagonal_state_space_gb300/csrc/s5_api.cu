@@ -264,7 +264,7 @@ s5_status s5_step(const float *lambda_bar, const float *b_bar, const float *c_ti
     const void *io[] = {x, u, y};
     for (const void *p : io)
         if (!p || !aligned16(p)) return S5_ERR_INVALID_ARGUMENT;
-    if (s5::step_smem_bytes(H, P) > 48 * 1024) return S5_ERR_UNSUPPORTED;
+    if (s5::step_smem_bytes(H, P) > 200 * 1024) return S5_ERR_UNSUPPORTED;
     cudaError_t e = s5::launch_step(reinterpret_cast<const float2 *>(lambda_bar), reinterpret_cast<const float2 *>(b_bar),
                                     reinterpret_cast<const float2 *>(c_tilde), d, reinterpret_cast<float2 *>(x), u, y,
                                     B, H, P, reinterpret_cast<cudaStream_t>(stream));

@@ -5,15 +5,18 @@
 // keeps just the current state per layer; summary "SIMPLIFIED STATE SPACE
 // LAYERS ...", App. C.1, online generation):
 //   x <- lambda_bar * x + B_bar u,   y = 2 Re(C~ x) + D u.
-// One block per sequence: u and the new state are staged in shared memory; a
-// warp per mode forms (B_bar u)_p with lanes striding over the features
-// (coalesced rows of B_bar), then a warp per feature forms the readout with
-// lanes striding over the modes.
+// One cluster of 8 CTAs per group of up to 8 sequences.  CTA r owns an eighth
+// of the modes: it reads its rows of B_bar once for all the group's sequences
+// and updates their states; after a cluster barrier every CTA gathers the new
+// states of all modes from its peers' shared memory (distributed shared
+// memory) and forms the readout for its eighth of the features.  So B_bar and
+// C~ are each read once per group rather than once per sequence.
 //
 // Bidirectional layer ("Simplified State Space Layers for Sequence Modeling",
 // "Paper vs code": a forward and a backward scan, C~ with 2P columns): the
 // helpers split C~ into its two [H,P] halves, reverse sequences in time and add
 // a time-reversed result into y.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "s5_internal.cuh"
@@ -21,7 +24,10 @@
 namespace s5 {
 namespace {
 
-constexpr int STEP_THREADS = 256;
+constexpr int STEP_THREADS = 512;
+constexpr int STEP_CL = 8;    // CTAs per cluster
+constexpr int STEP_SEQ = 8;   // sequences per cluster
+constexpr int STEP_KC = 4;    // row elements per lane fetched up front (rows of up to 128)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -29,46 +35,136 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__global__ void step_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restrict__ b_bar,
-                            const float2 *__restrict__ c_tilde, const float *__restrict__ d,
-                            float2 *__restrict__ x, const float *__restrict__ u, float *__restrict__ y, int H,
-                            int P) {
+// Warp w of a CTA takes modes p0 + w, p0 + w + 16, ... and features h0 + w,
+// h0 + w + 16, ...; for its first mode and feature every lane fetches its
+// elements of the B_bar and C~ rows (and the states, lambda_bar, D) before
+// anything else, so that one memory round trip covers them all.
+__global__ void __cluster_dims__(STEP_CL, 1, 1) __launch_bounds__(STEP_THREADS, 1)
+step_cluster_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restrict__ b_bar,
+                    const float2 *__restrict__ c_tilde, const float *__restrict__ d, float2 *__restrict__ x,
+                    const float *__restrict__ u, float *__restrict__ y, int B, int H, int P) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int r = (int)cl.block_rank();
+    const int s0 = (int)(blockIdx.x / STEP_CL) * STEP_SEQ;
+    const int ns = min(STEP_SEQ, B - s0);
+    const int mp = (P + STEP_CL - 1) / STEP_CL, hp = (H + STEP_CL - 1) / STEP_CL;
+    const int p0 = r * mp, p1 = min(P, p0 + mp), h0 = r * hp, h1 = min(H, h0 + hp);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     extern __shared__ float2 sm_step[];
-    float2 *sx = sm_step;                                // [P]
-    float *su = reinterpret_cast<float *>(sm_step + P);  // [H]
-    const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const float *ub = u + (size_t)b * H;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) su[h] = ub[h];
+    float2 *sx_own = sm_step;                                // [STEP_SEQ][mp]: this CTA's new states
+    float2 *sx_all = sx_own + STEP_SEQ * mp;                 // [STEP_SEQ][P]: every mode's new state
+    float *su = reinterpret_cast<float *>(sx_all + STEP_SEQ * P);   // [STEP_SEQ][H]
+
+    // everything the first mode and feature of this warp need, fetched at once
+    const int pf = p0 + warp, hf = h0 + warp;
+    float2 bw[STEP_KC], cw[STEP_KC];
+#pragma unroll
+    for (int k = 0; k < STEP_KC; ++k) {
+        const int h = lane + 32 * k, p = lane + 32 * k;
+        bw[k] = (pf < p1 && h < H) ? b_bar[(size_t)pf * H + h] : make_float2(0.f, 0.f);
+        cw[k] = (hf < h1 && p < P) ? c_tilde[(size_t)hf * P + p] : make_float2(0.f, 0.f);
+    }
+    float2 xo = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+    if (pf < p1 && lane < ns) {
+        xo = x[(size_t)(s0 + lane) * P + pf];
+        lb = lambda_bar[pf];
+    }
+    const float dh = hf < h1 ? d[hf] : 0.f;
+    for (int i = threadIdx.x; i < ns * H; i += blockDim.x) su[i] = u[(size_t)s0 * H + i];
     __syncthreads();
-    for (int p = warp; p < P; p += nwarps) {
-        const float2 *row = b_bar + (size_t)p * H;
-        float re = 0.f, im = 0.f;
-        for (int h = lane; h < H; h += 32) {
-            const float2 w = row[h];
-            re = fmaf(w.x, su[h], re);
-            im = fmaf(w.y, su[h], im);
+
+    // input projection, a warp per mode, all sequences at once
+    for (int p = pf; p < p1; p += nwarps) {
+        const bool first = p == pf;
+        float re[STEP_SEQ], im[STEP_SEQ];
+#pragma unroll
+        for (int q = 0; q < STEP_SEQ; ++q) re[q] = im[q] = 0.f;
+        for (int h = lane, k = 0; h < H; h += 32, ++k) {
+            float2 w;
+            if (first && k < STEP_KC) {
+                w = bw[0];
+#pragma unroll
+                for (int kk = 1; kk < STEP_KC; ++kk)
+                    if (k == kk) w = bw[kk];
+            } else {
+                w = b_bar[(size_t)p * H + h];
+            }
+#pragma unroll
+            for (int q = 0; q < STEP_SEQ; ++q)
+                if (q < ns) {
+                    const float v = su[q * H + h];
+                    re[q] = fmaf(w.x, v, re[q]);
+                    im[q] = fmaf(w.y, v, im[q]);
+                }
         }
-        re = warp_sum(re);
-        im = warp_sum(im);
-        if (lane == 0) {
-            const float2 lb = lambda_bar[p], xo = x[(size_t)b * P + p];
-            const float2 xn = make_float2(fmaf(lb.x, xo.x, fmaf(-lb.y, xo.y, re)), fmaf(lb.x, xo.y, fmaf(lb.y, xo.x, im)));
-            x[(size_t)b * P + p] = xn;
-            sx[p] = xn;
+        float bre = 0.f, bim = 0.f;
+#pragma unroll
+        for (int q = 0; q < STEP_SEQ; ++q) {
+            const float a = warp_sum(re[q]), c = warp_sum(im[q]);
+            if (lane == q) {
+                bre = a;
+                bim = c;
+            }
+        }
+        if (lane < ns) {
+            float2 xv = xo, lv = lb;
+            if (!first) {
+                xv = x[(size_t)(s0 + lane) * P + p];
+                lv = lambda_bar[p];
+            }
+            sx_own[lane * mp + (p - p0)] =
+                make_float2(fmaf(lv.x, xv.x, fmaf(-lv.y, xv.y, bre)), fmaf(lv.x, xv.y, fmaf(lv.y, xv.x, bim)));
         }
     }
-    __syncthreads();
-    for (int h = warp; h < H; h += nwarps) {
-        const float2 *row = c_tilde + (size_t)h * P;
-        float acc = 0.f;
-        for (int p = lane; p < P; p += 32) {
-            const float2 c = row[p], xv = sx[p];
-            acc = fmaf(c.x, xv.x, fmaf(-c.y, xv.y, acc));
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) y[(size_t)b * H + h] = fmaf(d[h], su[h], 2.f * acc);
+    // the barrier releases only shared-memory writes: the states go to global
+    // memory after it, so that it does not wait for those stores
+    cl.sync();
+    for (int i = threadIdx.x; i < ns * (p1 - p0); i += blockDim.x) {
+        const int q = i / (p1 - p0), pl = i - q * (p1 - p0);
+        x[(size_t)(s0 + q) * P + p0 + pl] = sx_own[q * mp + pl];
     }
+    // every mode's new state, from the CTA that owns it
+    for (int i = threadIdx.x; i < ns * P; i += blockDim.x) {
+        const int q = i / P, p = i - q * P, owner = p / mp;
+        const float2 *peer = cl.map_shared_rank(sx_own, owner);
+        sx_all[q * P + p] = peer[q * mp + (p - owner * mp)];
+    }
+    __syncthreads();
+    // readout, a warp per feature
+    for (int h = hf; h < h1; h += nwarps) {
+        const bool first = h == hf;
+        float acc[STEP_SEQ];
+#pragma unroll
+        for (int q = 0; q < STEP_SEQ; ++q) acc[q] = 0.f;
+        for (int p = lane, k = 0; p < P; p += 32, ++k) {
+            float2 c;
+            if (first && k < STEP_KC) {
+                c = cw[0];
+#pragma unroll
+                for (int kk = 1; kk < STEP_KC; ++kk)
+                    if (k == kk) c = cw[kk];
+            } else {
+                c = c_tilde[(size_t)h * P + p];
+            }
+#pragma unroll
+            for (int q = 0; q < STEP_SEQ; ++q)
+                if (q < ns) {
+                    const float2 xv = sx_all[q * P + p];
+                    acc[q] = fmaf(c.x, xv.x, fmaf(-c.y, xv.y, acc[q]));
+                }
+        }
+        float mine = 0.f;
+#pragma unroll
+        for (int q = 0; q < STEP_SEQ; ++q) {
+            const float a = warp_sum(acc[q]);
+            if (lane == q) mine = a;
+        }
+        if (lane < ns) y[(size_t)(s0 + lane) * H + h] = fmaf(first ? dh : d[h], su[lane * H + h], 2.f * mine);
+    }
+    // no CTA leaves while a peer may still read its states (their reads are
+    // complete once used, so the arrival need not order any memory access)
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // c2 [H][2P] -> cf [H][P] (columns 0..P-1), cb [H][P] (columns P..2P-1)
@@ -133,11 +229,21 @@ int grid_for(long long n) {
 
 }  // namespace
 
-size_t step_smem_bytes(int H, int P) { return sizeof(float2) * (size_t)P + sizeof(float) * (size_t)H; }
+size_t step_smem_bytes(int H, int P) {
+    const size_t mp = (size_t)(P + STEP_CL - 1) / STEP_CL;
+    return sizeof(float2) * STEP_SEQ * (mp + (size_t)P) + sizeof(float) * STEP_SEQ * (size_t)H;
+}
 
 cudaError_t launch_step(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_tilde, const float *d,
                         float2 *x, const float *u, float *y, int B, int H, int P, cudaStream_t st) {
-    step_kernel<<<B, STEP_THREADS, step_smem_bytes(H, P), st>>>(lambda_bar, b_bar, c_tilde, d, x, u, y, H, P);
+    const size_t smem = step_smem_bytes(H, P);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(step_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int clusters = (B + STEP_SEQ - 1) / STEP_SEQ;
+    step_cluster_kernel<<<clusters * STEP_CL, STEP_THREADS, smem, st>>>(lambda_bar, b_bar, c_tilde, d, x, u, y, B,
+                                                                        H, P);
     return cudaGetLastError();
 }
 

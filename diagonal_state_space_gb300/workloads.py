@@ -53,6 +53,10 @@ class Workload:
     proj_dtype: str = "f32"   # input type of the two projections
     varying_dt: bool = False  # per-step interval g_k * Delta_n
     bidirectional: bool = False  # forward and backward scans, C~ [H, 2P]
+    method: str = "zoh"       # discretisation: "zoh" or "bilinear"
+    clip_re: float = 0.0      # clip_eigs threshold on Re(lambda) (0: none)
+    dt_scale: float = 1.0     # sampling-rate factor on Delta (old rate / new rate)
+    streaming: bool = False   # one token per sequence per call (the step API), L calls
     layers: int = 0           # > 0: layer stack (pre-LN, SSM, gate, residual)
     seed: int = 0
     notes: str = field(default="", compare=False)
@@ -76,6 +80,13 @@ WORKLOADS = {
     "pathx_bf16_bidir": Workload("pathx_bf16_bidir", 8, 16384, 128, 128, u_dtype="bf16",
                                  proj_dtype="bf16", bidirectional=True, seed=2000,
                                  notes="the long-sequence shapes through the bidirectional layer"),
+    "pathx_bf16_bilinear": Workload("pathx_bf16_bilinear", 8, 16384, 128, 128, u_dtype="bf16",
+                                    proj_dtype="bf16", method="bilinear", clip_re=-1e-4,
+                                    dt_scale=0.5, seed=2000,
+                                    notes="the long-sequence shapes, bilinear discretisation with "
+                                          "clip_eigs and a doubled sampling rate"),
+    "stream": Workload("stream", 8, 1024, 128, 128, streaming=True, seed=4000,
+                       notes="streaming inference: 8 sequences, 1024 single-token steps, fp32"),
     "irregular": Workload("irregular", 32, 2048, 256, 128, varying_dt=True, seed=3000,
                           notes="per-step interval g_k*Delta_n, fp32"),
     "stack6": Workload("stack6", 32, 1024, 512, 256, u_dtype="f32", proj_dtype="bf16",

@@ -150,7 +150,8 @@ s5_status s5_forward_varying_dt(const float *lambda, const float *log_dt, const 
  *   u [B,H] float32 in; y [B,H] float32 out
  * Float32 throughout.  Errors: S5_ERR_INVALID_ARGUMENT for null/misaligned
  * pointers or B < 0, H < 1, P < 1; B = 0 is a no-op (x, u, y may then be
- * null); S5_ERR_UNSUPPORTED when 8P + 4H bytes of state and input exceed 48 KiB.
+ * null); S5_ERR_UNSUPPORTED when the 8 * (8 * (P + ceil(P/8)) + 4H) bytes of
+ * staged states and inputs exceed 200 KiB (about P, H > 2000).
  */
 s5_status s5_step(const float *lambda_bar, const float *b_bar, const float *c_tilde, const float *d,
                   float *x, const float *u, float *y, int B, int H, int P, s5_stream_t stream);

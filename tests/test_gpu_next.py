@@ -69,7 +69,10 @@ def test_discretize_ex_rejects_bad_options():
 # --------------------------------------------------------------------------
 # streaming step
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("B,H,P,steps", [(1, 1, 1, 3), (3, 32, 16, 20), (8, 128, 128, 8), (2, 300, 70, 5)])
+# several sequence groups (B > 8, ragged), P and H not multiples of 8, and a
+# size whose staged states need more than 48 KiB of shared memory
+@pytest.mark.parametrize("B,H,P,steps", [(1, 1, 1, 3), (3, 32, 16, 20), (8, 128, 128, 8), (2, 300, 70, 5),
+                                         (19, 64, 40, 3), (2, 1024, 1024, 2)])
 def test_step_matches_oracle(B, H, P, steps):
     inp = make_layer_inputs(B, steps, H, P, seed=21 + H)
     olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
