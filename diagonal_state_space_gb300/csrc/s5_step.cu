@@ -5,12 +5,13 @@
 // keeps just the current state per layer; summary "SIMPLIFIED STATE SPACE
 // LAYERS ...", App. C.1, online generation):
 //   x <- lambda_bar * x + B_bar u,   y = 2 Re(C~ x) + D u.
-// One cluster of 8 CTAs per group of up to 8 sequences.  CTA r owns an eighth
-// of the modes: it reads its rows of B_bar once for all the group's sequences
-// and updates their states; after a cluster barrier every CTA gathers the new
-// states of all modes from its peers' shared memory (distributed shared
-// memory) and forms the readout for its eighth of the features.  So B_bar and
-// C~ are each read once per group rather than once per sequence.
+// One cluster of 16 CTAs per group of up to 8 sequences.  CTA r owns a
+// sixteenth of the modes: it reads its rows of B_bar once for all the group's
+// sequences and updates their states; after a cluster barrier every CTA
+// gathers the new states of all modes from its peers' shared memory
+// (distributed shared memory) and forms the readout for its sixteenth of the
+// features.  So B_bar and C~ are each read once per group rather than once per
+// sequence, and every global load a warp needs is issued before any is used.
 //
 // Bidirectional layer ("Simplified State Space Layers for Sequence Modeling",
 // "Paper vs code": a forward and a backward scan, C~ with 2P columns): the
@@ -25,21 +26,38 @@ namespace s5 {
 namespace {
 
 constexpr int STEP_THREADS = 512;
-constexpr int STEP_CL = 8;    // CTAs per cluster
+constexpr int STEP_CL = 16;   // CTAs per cluster (a non-portable size)
 constexpr int STEP_SEQ = 8;   // sequences per cluster
 constexpr int STEP_KC = 4;    // row elements per lane fetched up front (rows of up to 128)
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sums each of N (a power of two, 2..32) per-lane values over the warp.  Each
+// exchange halves the values a lane holds: the lane keeps the half its lane
+// bit selects and adds its partner's copy of that half.  Afterwards lane l
+// holds the total of value l / (32 / N) (the 32 / N lanes of a group agree).
+template <int N>
+__device__ __forceinline__ float warp_sum_many(float (&v)[N]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int half = N / 2, o = 16; half >= 1; half /= 2, o /= 2) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+            const float keep = up ? v[j + half] : v[j];
+            const float send = up ? v[j] : v[j + half];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 / N; o >= 1; o /= 2) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
 }
 
 // Warp w of a CTA takes modes p0 + w, p0 + w + 16, ... and features h0 + w,
 // h0 + w + 16, ...; for its first mode and feature every lane fetches its
 // elements of the B_bar and C~ rows (and the states, lambda_bar, D) before
 // anything else, so that one memory round trip covers them all.
-__global__ void __cluster_dims__(STEP_CL, 1, 1) __launch_bounds__(STEP_THREADS, 1)
+__global__ void __launch_bounds__(STEP_THREADS, 1)
 step_cluster_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restrict__ b_bar,
                     const float2 *__restrict__ c_tilde, const float *__restrict__ d, float2 *__restrict__ x,
                     const float *__restrict__ u, float *__restrict__ y, int B, int H, int P) {
@@ -98,15 +116,16 @@ step_cluster_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restr
                     im[q] = fmaf(w.y, v, im[q]);
                 }
         }
-        float bre = 0.f, bim = 0.f;
+        // values 0..7: Re for the eight sequences, 8..15: Im; lane 2j holds value j
+        float v[2 * STEP_SEQ];
 #pragma unroll
         for (int q = 0; q < STEP_SEQ; ++q) {
-            const float a = warp_sum(re[q]), c = warp_sum(im[q]);
-            if (lane == q) {
-                bre = a;
-                bim = c;
-            }
+            v[q] = re[q];
+            v[STEP_SEQ + q] = im[q];
         }
+        const float tot = warp_sum_many(v);
+        const float bre = __shfl_sync(0xffffffffu, tot, 2 * lane);
+        const float bim = __shfl_sync(0xffffffffu, tot, 2 * (STEP_SEQ + lane) & 31);
         if (lane < ns) {
             float2 xv = xo, lv = lb;
             if (!first) {
@@ -154,12 +173,8 @@ step_cluster_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restr
                     acc[q] = fmaf(c.x, xv.x, fmaf(-c.y, xv.y, acc[q]));
                 }
         }
-        float mine = 0.f;
-#pragma unroll
-        for (int q = 0; q < STEP_SEQ; ++q) {
-            const float a = warp_sum(acc[q]);
-            if (lane == q) mine = a;
-        }
+        // lane 4q holds sequence q's sum
+        const float mine = __shfl_sync(0xffffffffu, warp_sum_many(acc), (4 * lane) & 31);
         if (lane < ns) y[(size_t)(s0 + lane) * H + h] = fmaf(first ? dh : d[h], su[lane * H + h], 2.f * mine);
     }
     // no CTA leaves while a peer may still read its states (their reads are
@@ -241,10 +256,22 @@ cudaError_t launch_step(const float2 *lambda_bar, const float2 *b_bar, const flo
         cudaError_t e = cudaFuncSetAttribute(step_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
+    cudaError_t e = cudaFuncSetAttribute(step_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     const int clusters = (B + STEP_SEQ - 1) / STEP_SEQ;
-    step_cluster_kernel<<<clusters * STEP_CL, STEP_THREADS, smem, st>>>(lambda_bar, b_bar, c_tilde, d, x, u, y, B,
-                                                                        H, P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(clusters * STEP_CL));
+    cfg.blockDim = dim3(STEP_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = STEP_CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, step_cluster_kernel, lambda_bar, b_bar, c_tilde, d, x, u, y, B, H, P);
 }
 
 cudaError_t launch_split_c(const float2 *c2, int H, int P, float2 *cf, float2 *cb, cudaStream_t st) {
