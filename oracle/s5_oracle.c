@@ -27,7 +27,7 @@
  * interleaved (re, im) pairs, which is the memory layout of C99
  * `double complex`.
  *
- * Readings of points the pages leave open (each listed in the design doc):
+ * Readings of points the pages leave open:
  *  - the readout takes 2*Re(C x) for every stored mode and adds D*u once;
  *  - time index k = 1..L with x_0 = 0 (or the caller's x0), so y_1 already
  *    contains B-bar u_1;
