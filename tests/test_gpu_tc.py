@@ -34,8 +34,10 @@ def _run(B, L, seed, zero_d=False, x0=None):
     return host(y), oy, host(xl), oxl
 
 
+# (60, 130): fewer than two CTAs per sequence fit, so each CTA takes whole
+# sequences with the carry in registers; (160, 65): more sequences than SMs
 @pytest.mark.parametrize("B,L", [(1, 64), (1, 1), (1, 63), (1, 65), (2, 128), (3, 1000),
-                                 (8, 4097), (1, 20000)])
+                                 (8, 4097), (1, 20000), (60, 130), (160, 65)])
 @pytest.mark.parametrize("zero_d", [False, True])
 def test_tc_forward_matches_oracle(B, L, zero_d):
     y, oy, xl, oxl = _run(B, L, seed=31 * B + L, zero_d=zero_d)
