@@ -355,7 +355,8 @@ def run_ours(args):
     if w.bidirectional:
         # the timed call is the whole bidirectional layer: two forward launches
         # plus the split / reverse / add kernels; no single-kernel DRAM capture
-        kname = "bidirectional layer (2 x %s + split, reverse, add)" % kname
+        kname = ("bidirectional layer (fwd_tc_kernel + bwd_tc_kernel + split)" if tc_path else
+                 "bidirectional layer (2 x %s + split, reverse, add)" % kname)
         traffic = None
     result = {
         "metric": BIDI_METRIC if w.bidirectional else METRIC,
@@ -408,8 +409,9 @@ def run_ours(args):
                 "ms_per_step": e2e_ms},
         # per step: discretize + (weight images + tensor-core forward | CUDA-core forward),
         # or, with per-step intervals, mode constants + CUDA-core forward
-        # bidirectional: discretize, split, reverse, 2 x (images + forward | forward), add
-        "gpu_launches": args.steps * ((8 if tc_path else 6) if w.bidirectional else (3 if tc_path else 2)),
+        # bidirectional, tensor-core path: discretize, split, 2 x (images + scan kernel);
+        # CUDA-core path: discretize, split, reverse, 2 x forward, add
+        "gpu_launches": args.steps * (6 if w.bidirectional else (3 if tc_path else 2)),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -150,6 +150,32 @@ s5_status run_tc(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_
     return e == cudaSuccess ? S5_OK : cuda_fail(e);
 }
 
+// The backward scan of the bidirectional layer on the tensor-core path: adds
+// 2 Re(c_tilde_b xb_k) into y, scanning each sequence from its end.
+s5_status run_tc_backward_add(const float2 *lambda_bar, const float2 *b_bar, const float2 *c_tilde_b,
+                              const void *u, void *y, int B, int L, int P, void *workspace, cudaStream_t st) {
+    const int sms = num_sms_current();
+    if (sms == 0) return cuda_fail(cudaGetLastError());
+    const long long nchunks = ceil_div(L, s5::TC_TILE_TOKENS);
+    const long long ntiles = nchunks * B;
+    if (ntiles >= (1ll << 31)) return S5_ERR_UNSUPPORTED;
+    s5::TcArgs a;
+    a.lambda_bar = lambda_bar;
+    a.b_bar = b_bar;
+    a.c_tilde = c_tilde_b;
+    a.d = nullptr;
+    a.y = y;
+    a.x0 = nullptr;
+    a.x_last = nullptr;
+    a.B = B;
+    a.L = L;
+    a.nchunks = (int)nchunks;
+    a.ntiles = (int)ntiles;
+    a.ws = s5::ws_layout(workspace, ntiles, P);
+    cudaError_t e = s5::launch_backward_add_tc(a, u, st, sms);
+    return e == cudaSuccess ? S5_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -317,7 +343,17 @@ s5_status s5_forward_bidirectional(const float *lambda_bar, const float *b_bar, 
     float2 *cf = reinterpret_cast<float2 *>(w + l.cf), *cb = reinterpret_cast<float2 *>(w + l.cb);
     float *d0 = reinterpret_cast<float *>(w + l.d0);
     cudaError_t e = s5::launch_split_c(reinterpret_cast<const float2 *>(c_tilde2), H, P, cf, cb, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d0, 0, sizeof(float) * (size_t)H, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (s5::tc_supported(H, P, u_dtype == S5_BF16, y_dtype == S5_BF16, proj_dtype == S5_BF16)) {
+        // tensor-core path: the forward scan writes y, the backward scan adds
+        // into it in place (no reversed copies)
+        s5_status s = s5_forward(lambda_bar, b_bar, reinterpret_cast<const float *>(cf), d, u, u_dtype, y,
+                                 y_dtype, proj_dtype, B, L, H, P, nullptr, nullptr, w, l.fwd, stream);
+        if (s != S5_OK) return s;
+        return run_tc_backward_add(reinterpret_cast<const float2 *>(lambda_bar),
+                                   reinterpret_cast<const float2 *>(b_bar), cb, u, y, B, L, P, w, st);
+    }
+    e = cudaMemsetAsync(d0, 0, sizeof(float) * (size_t)H, st);
     if (e == cudaSuccess)
         e = s5::launch_reverse_time(u, w + l.ur, B, L, H, u_dtype == S5_BF16 ? 2 : 4, st);
     if (e != cudaSuccess) return cuda_fail(e);

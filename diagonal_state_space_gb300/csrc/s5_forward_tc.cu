@@ -43,6 +43,16 @@
 // leave the SM.  All waits are bounded; a wait that runs out latches
 // S5_ERR_TIMEOUT, stops the CTA's pipeline, drains its copies and MMAs and
 // frees its TMEM.
+// Compiled twice.  S5_TC_REV = 0 (this file): the layer's forward scan.
+// S5_TC_REV = 1 (s5_backward_tc.cu includes this file): the backward scan of
+// the bidirectional layer -- chunks and the tokens inside a tile are visited
+// in reverse (scan position q is chunk nchunks-1-q, token 63-s of a full
+// tile), x0 and x_last are not used, and the epilogue adds the readout to the
+// y already there: its second TMA copy reads y instead of u.  Every
+// difference sits in an "#if S5_TC_REV" block.
+#ifndef S5_TC_REV
+#define S5_TC_REV 0
+#endif
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -311,12 +321,22 @@ __device__ __forceinline__ float2 pass1_full(uint32_t col0, const ScanConsts &k,
         uint32_t re[4][4], im[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+#if S5_TC_REV
+            tmem_ld4(col0 + 60 - 16 * q - 4 * r, re[q]);
+            tmem_ld4(col0 + 64 + 60 - 16 * q - 4 * r, im[q]);
+#else
             tmem_ld4(col0 + 16 * q + 4 * r, re[q]);
             tmem_ld4(col0 + 64 + 16 * q + 4 * r, im[q]);
+#endif
         }
         tmem_wait_ld();
 #pragma unroll
+#if S5_TC_REV
+        for (int tt = 0; tt < 4; ++tt) {
+            const int t = 3 - tt;
+#else
         for (int t = 0; t < 4; ++t) {
+#endif
             c0 = cfma(k.lb, c0, make_float2(__uint_as_float(re[0][t]), __uint_as_float(im[0][t])));
             c1 = cfma(k.lb, c1, make_float2(__uint_as_float(re[1][t]), __uint_as_float(im[1][t])));
             c2 = cfma(k.lb, c2, make_float2(__uint_as_float(re[2][t]), __uint_as_float(im[2][t])));
@@ -333,14 +353,22 @@ __device__ __forceinline__ float2 pass1_full(uint32_t col0, const ScanConsts &k,
 __device__ __noinline__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
     float2 e = make_float2(0.f, 0.f);
 #pragma unroll 1
+#if S5_TC_REV
+    for (int ch = (Tc - 1) / 16; ch >= 0; --ch) {
+#else
     for (int ch = 0; ch * 16 < Tc; ++ch) {
+#endif
         uint32_t re[16], im[16];
         tmem_ld16(col0 + ch * 16, re);
         tmem_ld16(col0 + 64 + ch * 16, im);
         tmem_wait_ld();
         const int n = Tc - ch * 16;
 #pragma unroll
+#if S5_TC_REV
+        for (int t = 15; t >= 0; --t)
+#else
         for (int t = 0; t < 16; ++t)
+#endif
             if (t < n) e = cfma(lb, e, make_float2(__uint_as_float(re[t]), __uint_as_float(im[t])));
     }
     return e;
@@ -369,24 +397,43 @@ __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)
         uint32_t re[4][4], im[4][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+#if S5_TC_REV
+            tmem_ld4(col0 + 60 - 16 * q - 4 * r, re[q]);
+            tmem_ld4(col0 + 64 + 60 - 16 * q - 4 * r, im[q]);
+#else
             tmem_ld4(col0 + 16 * q + 4 * r, re[q]);
             tmem_ld4(col0 + 64 + 16 * q + 4 * r, im[q]);
+#endif
         }
         tmem_wait_ld();
         if (r == 3) bu_read_done(done);
         const uint32_t o = (uint32_t)(r >> 1) * 1024u;
         const int t0 = (r & 1) * 4;
 #pragma unroll
+#if S5_TC_REV
+        // scan position 16q + 4r + tt is token and X row 63 - (16q + 4r + tt)
+        for (int tt = 0; tt < 4; ++tt) {
+            const int t = 3 - tt;
+#else
         for (int t = 0; t < 4; ++t) {
+#endif
             s0 = cfma(k.lb, s0, make_float2(__uint_as_float(re[0][t]), __uint_as_float(im[0][t])));
             s1 = cfma(k.lb, s1, make_float2(__uint_as_float(re[1][t]), __uint_as_float(im[1][t])));
             s2 = cfma(k.lb, s2, make_float2(__uint_as_float(re[2][t]), __uint_as_float(im[2][t])));
             s3 = cfma(k.lb, s3, make_float2(__uint_as_float(re[3][t]), __uint_as_float(im[3][t])));
+#if S5_TC_REV
+            const uint32_t a = ((r & 1) ? xb[3 - tt] : xb[7 - tt]) + 7168u - o;
+            sts32(a, pack_bf16(s0.x, s0.y));
+            sts32(a - 2048u, pack_bf16(s1.x, s1.y));
+            sts32(a - 4096u, pack_bf16(s2.x, s2.y));
+            sts32(a - 6144u, pack_bf16(s3.x, s3.y));
+#else
             const uint32_t a = ((r & 1) ? xb[4 + t] : xb[t]) + o;
             sts32(a, pack_bf16(s0.x, s0.y));
             sts32(a + 2048u, pack_bf16(s1.x, s1.y));
             sts32(a + 4096u, pack_bf16(s2.x, s2.y));
             sts32(a + 6144u, pack_bf16(s3.x, s3.y));
+#endif
         }
         (void)t0;
     }
@@ -397,7 +444,11 @@ __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)
 __device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb, float2 x, int Tc,
                                             uint64_t *done) {
 #pragma unroll 1
+#if S5_TC_REV
+    for (int ch = T_TOK / 16 - 1; ch >= 0; --ch) {
+#else
     for (int ch = 0; ch < T_TOK / 16; ++ch) {
+#endif
         uint32_t re[16], im[16];
         const bool live = ch * 16 < Tc;
         if (live) {
@@ -406,7 +457,11 @@ __device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8
             tmem_wait_ld();
         }
 #pragma unroll
+#if S5_TC_REV
+        for (int t = 15; t >= 0; --t) {
+#else
         for (int t = 0; t < 16; ++t) {
+#endif
             uint32_t pv = 0;
             if (live && ch * 16 + t < Tc) {
                 x = cfma(lb, x, make_float2(__uint_as_float(re[t]), __uint_as_float(im[t])));
@@ -433,7 +488,11 @@ __device__ __forceinline__ bool scan_front(ScanTile &T, int i, const Lane &ln, i
     int b, c;
     ln.tile(i, b, c);
     const int g = b * ln.nchunks + c, r = i % REGIONS;
+#if S5_TC_REV
+    T.Tc = min(T_TOK, L - (ln.nchunks - 1 - c) * T_TOK);
+#else
     T.Tc = min(T_TOK, L - c * T_TOK);
+#endif
     if (!pipe_wait(&sb->tmem_full[r], (i / REGIONS) & 1, sb, hdr)) return false;
     tc_fence_after();
     const uint32_t col0 = lane_base + (uint32_t)r * 128u;
@@ -474,7 +533,12 @@ __global__ void weight_images_kernel(const float2 *__restrict__ b_bar, const flo
 // Main kernel.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(THREADS, 1)
+#if S5_TC_REV
+bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const __grid_constant__ CUtensorMap tmap_e,
+              const TcArgs args) {
+#else
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
+#endif
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     unsigned char *smem = smem_raw + pad;
@@ -562,8 +626,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                 int b, c;
                 ln.tile(i, b, c);
                 mbar_arrive_tx(&sb->eu_full, U_STAGE);
+#if S5_TC_REV
+                c = nchunks - 1 - c;
+                tma_load_3d(smem + SM_EU, &tmap_e, 0, c * T_TOK, b, &sb->eu_full);
+                tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_e, 64, c * T_TOK, b, &sb->eu_full);
+#else
                 tma_load_3d(smem + SM_EU, &tmap_u, 0, c * T_TOK, b, &sb->eu_full);
                 tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->eu_full);
+#endif
                 last = i;
             }
             // the copy in flight must land before the CTA exits
@@ -580,6 +650,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             const uint32_t xs = smem_addr(smem + SM_X);
             if (warp == 0) {
                 prefetch_tmap(&tmap_u);
+#if S5_TC_REV
+                prefetch_tmap(&tmap_e);
+#endif
                 mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
                 bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
                 bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
@@ -590,6 +663,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                     if (il >= STAGES && !pipe_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1, sb, hdr)) break;
                     int b, c;
                     ln.tile(il, b, c);
+#if S5_TC_REV
+                    c = nchunks - 1 - c;
+#endif
                     unsigned char *dst = smem + SM_U + s * U_STAGE;
                     mbar_arrive_tx(&sb->full_u[s], U_STAGE);
                     tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
@@ -733,7 +809,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         // is released once its last column is in registers.
         const int qd = warp - W_EPI;
         const int h = 32 * qd + lane;
+#if S5_TC_REV
+        const float dh = 1.f;   // the copy holds y, which is added
+#else
         const float dh = args.d[h];
+#endif
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         unsigned short *yout = static_cast<unsigned short *>(args.y);
         // this feature's u for token t: row t, column h of the swizzled copy
@@ -743,6 +823,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             const int r = i % REGIONS;
             int b, c;
             ln.tile(i, b, c);
+#if S5_TC_REV
+            c = nchunks - 1 - c;
+#endif
             const int Tc = min(T_TOK, L - c * T_TOK);
             const size_t row0 = ((size_t)b * L + (size_t)c * T_TOK) * H_F + h;
             unsigned short *yrow = yout + row0;
@@ -844,6 +927,7 @@ bool make_map(CUtensorMap *map, const void *base, int B, int L) {
 
 }  // namespace
 
+#if !S5_TC_REV
 bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16) {
     return H == H_F && P == P_M && u_bf16 && y_bf16 && proj_bf16;
 }
@@ -896,5 +980,41 @@ cudaError_t launch_forward_tc(const TcArgs &a0, const void *u, cudaStream_t st, 
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fwd_tc_kernel, mu, a);
 }
+
+#else
+cudaError_t launch_backward_add_tc(const TcArgs &a0, const void *u, cudaStream_t st, int num_sms) {
+    TcArgs a = a0;
+    a.u = u;
+    a.x0 = nullptr;
+    a.x_last = nullptr;
+    int G = 0;
+    tc_grid(a.B, a.nchunks, num_sms, &a.W, &G);
+    CUtensorMap mu, my;
+    if (!make_map(&mu, u, a.B, a.L)) return cudaErrorInvalidValue;
+    if (!make_map(&my, a.y, a.B, a.L)) return cudaErrorInvalidValue;
+    const int words = P_M * H_F / 2 + H_F * P_M;
+    weight_images_kernel<<<(words + 255) / 256, 256, 0, st>>>(a.b_bar, a.c_tilde, a.ws.wimg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_REQUEST);
+    if (e != cudaSuccess) return e;
+    // cooperative launch, as for the forward scan
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_tc_kernel, THREADS, SMEM_REQUEST);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_REQUEST;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_tc_kernel, mu, my, a);
+}
+#endif
 
 }  // namespace s5

@@ -22,6 +22,12 @@ struct TcArgs {
 
 // The tensor-core kernel covers H = 128, P = 128 with bf16 u, y and projections.
 bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16);
+// Lanes per sequence (W) and grid size (G) of the tensor-core launches.
+void tc_grid(int B, int nchunks, int num_sms, int *W, int *G);
 cudaError_t launch_forward_tc(const TcArgs &a, const void *u, cudaStream_t st, int num_sms);
+// The backward scan of the bidirectional layer (a.c_tilde = the backward
+// half of C~; a.d, a.x0, a.x_last unused): y += 2 Re(C~_b xb), with
+// xb_k = lambda_bar xb_{k+1} + B_bar u_k over each sequence in reverse.
+cudaError_t launch_backward_add_tc(const TcArgs &a, const void *u, cudaStream_t st, int num_sms);
 
 }  // namespace s5

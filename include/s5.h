@@ -168,9 +168,14 @@ s5_status s5_step(const float *lambda_bar, const float *b_bar, const float *c_ti
  *   s5_forward (the same kernel path is chosen for both scans).
  *   workspace: at least s5_bidirectional_workspace_size(B,L,H,P,u_dtype,y_dtype)
  *   bytes, zero-filled before its first use.
- * Runs as: the two halves of c_tilde2 split into [H,P] arrays, u reversed in
- * time, s5_forward on u (with d) and on the reversed u (with d = 0), and the
- * second result reversed and added into y -- all on `stream`.
+ * Runs as (all on `stream`): the two halves of c_tilde2 split into [H,P]
+ * arrays; then
+ *  - tensor-core shapes (H = P = 128, bf16 u, y and projections): s5_forward
+ *    on u with the first half and d, then one more launch of the same kernel
+ *    that scans every sequence from its end with the second half and adds its
+ *    readout into y in place;
+ *  - other shapes: u reversed in time, s5_forward on u (with d) and on the
+ *    reversed u (with d = 0), and the second result reversed and added into y.
  * Errors: those of s5_forward; S5_ERR_UNSUPPORTED when B*L*H >= 2^31.
  */
 s5_status s5_forward_bidirectional(const float *lambda_bar, const float *b_bar, const float *c_tilde2,

@@ -140,7 +140,9 @@ def test_bidirectional_f32_matches_oracle(B, L, H, P):
         assert rel_l2(host(y), oy) <= FP32_TOL, (dz, rel_l2(host(y), oy))
 
 
-@pytest.mark.parametrize("B,L", [(2, 700), (1, 4096)])
+# ragged last chunk (the backward scan's first), many lanes per sequence, one
+# lane per sequence (B = 60), several sequences per CTA (B = 160)
+@pytest.mark.parametrize("B,L", [(2, 700), (1, 4096), (1, 1), (60, 130), (160, 65)])
 def test_bidirectional_bf16_tensor_core_path_matches_oracle(B, L):
     H = P = 128
     inp = make_layer_inputs(B, L, H, P, seed=41 + L, u_dtype="bf16")
