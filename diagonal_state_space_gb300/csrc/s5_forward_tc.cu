@@ -229,7 +229,8 @@ struct Lane {
 };
 
 // Waits (bounded) until the 16-byte record at p carries `tag`; returns its
-// value.  A wait that runs out latches S5_ERR_TIMEOUT (once per thread) and
+// value.  The record is re-read back to back (each read is one L2 round
+// trip): a sleep between reads measurably delays the carries.  A wait that runs out latches S5_ERR_TIMEOUT (once per thread) and
 // returns zero, so that the launch still completes.
 __device__ float2 wait_record(const float4 *p, unsigned tag, WsHeader *hdr, unsigned long long limit,
                               bool &gave_up, unsigned tile) {
@@ -237,7 +238,6 @@ __device__ float2 wait_record(const float4 *p, unsigned tag, WsHeader *hdr, unsi
     if (__float_as_uint(v.w) == tag) return make_float2(v.x, v.y);
     const unsigned long long t0 = global_ns();
     while (!gave_up) {
-        __nanosleep(64);
         v = ld_record(p);
         if (__float_as_uint(v.w) == tag) return make_float2(v.x, v.y);
         if (global_ns() - t0 > limit) {
@@ -296,7 +296,6 @@ __device__ __noinline__ void scanner_loop(const float4 *agg, float4 *carry, size
                 atomicCAS(&hdr->timeout_tile, 0u, (unsigned)(seq + q0 + done) + 1u);
                 gave_up = true;
             }
-            __nanosleep(32);
         }
     }
 }
