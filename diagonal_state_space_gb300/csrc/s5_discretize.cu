@@ -55,11 +55,19 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
     const int p = blockIdx.x;
     __shared__ double s_f[5];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2)
     __shared__ double s_gain[2];
-    const float2 l = lambda[p];
-    dcplx lam = {(double)l.x, (double)l.y};
-    if (clip_re != 0.0 && lam.re > clip_re) lam.re = clip_re;
-    const double dt = exp((double)log_dt[p]) * dt_scale;
-    const dcplx z = {lam.re * dt, lam.im * dt};
+    // Only the first lane of each of the first four warps needs Delta and z:
+    // float64 work on the other lanes would still occupy the SM's few float64
+    // units, so they skip it.
+    const bool leader = (threadIdx.x & 31) == 0 && threadIdx.x < 128;
+    dcplx lam = {0.0, 0.0}, z = {0.0, 0.0};
+    double dt = 0.0;
+    if (leader) {
+        const float2 l = lambda[p];
+        lam = {(double)l.x, (double)l.y};
+        if (clip_re != 0.0 && lam.re > clip_re) lam.re = clip_re;
+        dt = exp((double)log_dt[p]) * dt_scale;
+        z = {lam.re * dt, lam.im * dt};
+    }
     if (method == 1) {
         if (threadIdx.x == 0) {
             const dcplx den = {1.0 - 0.5 * z.re, -0.5 * z.im};
@@ -69,7 +77,7 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
             s_gain[0] = gain.re;
             s_gain[1] = gain.im;
         }
-    } else if ((threadIdx.x & 31) == 0) {
+    } else if (leader) {
         const int w = threadIdx.x >> 5;
         if (w == 0) sincos(z.im, &s_f[0], &s_f[1]);
         else if (w == 1) s_f[2] = exp(z.re);
