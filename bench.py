@@ -290,44 +290,71 @@ def run_ours(args):
     tokens = w.B * w.L
     value = tokens * world / (ms_step / 1e3)
 
-    # end-to-end through the public API with host buffers
+    # End to end through the public API with host buffers: every step copies
+    # all its inputs (u and the parameters) in from pinned host memory and its
+    # output y back out, inside the timed region.  Two device buffer sets and
+    # two copy streams let step i's copies overlap step i-1's compute -- how a
+    # caller streaming batches runs it; the compute calls are the same.
     u_host = torch.from_numpy(np.ascontiguousarray(inp["u"])).to(u_dt).pin_memory()
-    y_host = torch.empty(u_host.shape, dtype=u_dt).pin_memory()
+    y_hosts = [torch.empty(u_host.shape, dtype=u_dt).pin_memory() for _ in range(2)]
     host_params = [torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
                    for k in ("lambda_", "log_dt", "b_tilde",
                              "c_tilde2" if w.bidirectional else "c_tilde", "d")]
     if w.varying_dt:
         host_params.append(torch.from_numpy(np.ascontiguousarray(inp["g"])).pin_memory())
-    dev_params = [torch.empty_like(p, device="cuda") for p in host_params]
-    u_dev, y_dev = u_sets[0], y_sets[0]
+    dev_params = [[torch.empty_like(p, device="cuda") for p in host_params] for _ in range(2)]
+    u_devs, y_devs = u_sets[:2], y_sets[:2]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
-        u_dev.copy_(u_host, non_blocking=True)
-        for hp, dp in zip(host_params, dev_params):
-            dp.copy_(hp, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if used[k]:
+                s_in.wait_event(ev_cmp[k])      # set k is free once step i-2 has computed
+            u_devs[k].copy_(u_host, non_blocking=True)
+            for hp, dp in zip(host_params, dev_params[k]):
+                dp.copy_(hp, non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        if used[k]:
+            stream.wait_event(ev_out[k])        # y set k has been read back by step i-2
+        dp, u_dev, y_dev = dev_params[k], u_devs[k], y_devs[k]
         if w.varying_dt:
-            api.s5_forward_varying_dt(*dev_params[:5], dev_params[5], u_dev, y=y_dev,
-                                      proj_dtype=w.proj_dtype, workspace=ws)
+            api.s5_forward_varying_dt(*dp[:5], dp[5], u_dev, y=y_dev, proj_dtype=w.proj_dtype,
+                                      workspace=ws)
         else:
-            l_, b_ = discretize(dev_params[0], dev_params[1], dev_params[2])
+            l_, b_ = discretize(dp[0], dp[1], dp[2])
             if w.bidirectional:
-                api.s5_forward_bidirectional(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
+                api.s5_forward_bidirectional(l_, b_, dp[3], dp[4], u_dev, y=y_dev,
                                              proj_dtype=w.proj_dtype, workspace=ws)
             else:
-                api.s5_forward(l_, b_, dev_params[3], dev_params[4], u_dev, y=y_dev,
-                               proj_dtype=w.proj_dtype, workspace=ws)
-        y_host.copy_(y_dev, non_blocking=True)
+                api.s5_forward(l_, b_, dp[3], dp[4], u_dev, y=y_dev, proj_dtype=w.proj_dtype,
+                               workspace=ws)
+        ev_cmp[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[k])
+            y_hosts[k].copy_(y_dev, non_blocking=True)
+            ev_out[k].record(s_out)
+        used[k] = True
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(3, 3 + args.e2e_steps):
+        e2e_step(i)
+    stream.wait_event(ev_out[0])
+    stream.wait_event(ev_out[1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -335,6 +362,7 @@ def run_ours(args):
         tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
+    y_host = y_hosts[0]
     h2d = u_host.numel() * u_host.element_size() + sum(p.numel() * p.element_size()
                                                        for p in host_params)
     d2h = y_host.numel() * y_host.element_size()
@@ -406,7 +434,9 @@ def run_ours(args):
         },
         "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "note": "public API, pinned host buffers; two device sets and two copy "
+                        "streams overlap step i's copies with step i-1's compute"},
         # per step: discretize + (weight images + tensor-core forward | CUDA-core forward),
         # or, with per-step intervals, mode constants + CUDA-core forward
         # bidirectional, tensor-core path: discretize, split, 2 x (images + scan kernel);
