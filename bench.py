@@ -68,6 +68,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms, dist, device="cuda"):
+    """The slowest rank's time: the job is done when its last replica is."""
+    if not dist:
+        return ms
+    import torch
+    tt = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job rate: every rank's units over the slowest rank's time (ms)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -277,10 +292,7 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ms_total = t_start.elapsed_time(t_end)
-    if dist:
-        tt = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dist)
     st = api.s5_sync_status(ws)
     if st != 0:
         raise RuntimeError("device status %d after the timed region" % st)
@@ -288,7 +300,7 @@ def run_ours(args):
     fwd_avg_s = statistics.fmean(fwd_ms) / 1e3
     ms_step = ms_total / args.steps
     tokens = w.B * w.L
-    value = tokens * world / (ms_step / 1e3)
+    value = job_throughput(tokens, world, ms_step)
 
     # End to end through the public API with host buffers: every step copies
     # all its inputs (u and the parameters) in from pinned host memory and its
@@ -358,10 +370,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     y_host = y_hosts[0]
     h2d = u_host.numel() * u_host.element_size() + sum(p.numel() * p.element_size()
                                                        for p in host_params)
@@ -432,7 +441,7 @@ def run_ours(args):
             "launch_us": fwd_avg_s * 1e6,
             "traffic": traffic,
         },
-        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
                 "note": "public API, pinned host buffers; two device sets and two copy "
@@ -513,14 +522,11 @@ def run_stream(args):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ms_total = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dist)
     ms_step = ms_total / args.steps
     call_s = statistics.fmean(a.elapsed_time(b) for a, b in loop_ev) / 1e3 / w.L
     tokens = w.B * w.L
-    value = tokens * world / (ms_step / 1e3)
+    value = job_throughput(tokens, world, ms_step)
 
     # end to end: host u in, host y out, every call through the public API
     u_host = torch.from_numpy(np.ascontiguousarray(np.transpose(inp["u"], (1, 0, 2)))).pin_memory()
@@ -547,10 +553,7 @@ def run_stream(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     h2d = u_host.numel() * 4 + sum(p.numel() * p.element_size() for p in host_params)
     d2h = y_host.numel() * 4
     if rank != 0:
@@ -585,7 +588,7 @@ def run_stream(args):
             "algorithmic_bytes_per_launch": alg, "launch_us": call_s * 1e6, "traffic": None,
             "note": "a dependent chain of small launches: bound by launch latency, not bandwidth",
         },
-        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * (1 + w.L),
         "clocks": clocks,
@@ -653,10 +656,7 @@ def run_stack(args):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        tt = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dist)
     tokens = w.B * w.L
     # end to end: u0 and G from pinned host memory, du0 back
     u_host = torch.from_numpy(np.ascontiguousarray(inp["u0"])).pin_memory()
@@ -687,7 +687,7 @@ def run_stack(args):
     flops = stack_flops(w.B, w.L, w.H, w.P, w.layers)
     achieved = flops / (ms / 1e3) / 1e12
     result = {
-        "metric": STACK_METRIC, "value": tokens * world / (ms / 1e3), "unit": "tokens/s",
+        "metric": STACK_METRIC, "value": job_throughput(tokens, world, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64 per layer)",
@@ -703,7 +703,7 @@ def run_stack(args):
                      "frac": achieved / bf16_tf if bf16_tf else None,
                      "peak_source": "%s (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
                      "flops_per_step": flops, "traffic": None},
-        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * u_host.numel() * 4, "d2h_bytes_per_step": du_host.numel() * 4,
                 "ms_per_step": e2e_ms},
         # per step one discretize of all layers' modes; per layer: forward weights,
