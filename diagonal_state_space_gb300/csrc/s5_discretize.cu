@@ -32,10 +32,11 @@ __device__ inline dcplx ddiv(dcplx a, dcplx b) {
 //   every thread  dt = exp(log_dt)
 //   warp 0  sin(Im z), cos(Im z)      warp 1  exp(Re z)
 //   warp 2  expm1(Re z)               warp 3  sin(Im z / 2)
+//   warp 4  1 / lambda
 // then lambda_bar = e^Re z (cos, sin) and, for |z| >= 1e-4,
-// (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z))/lambda;
+// (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z)) * (1/lambda);
 // below |z| = 1e-4, Delta * phi1(z) from its Taylor series.  Every thread of
-// the block then scales a slice of the B_tilde row.  Blocks have >= 128 threads.
+// the block then scales a slice of the B_tilde row.  Blocks have >= 160 threads.
 //
 // Options (all in float64, applied before the factors above):
 //   clip_re != 0   clip_eigs: Re(lambda) <- min(Re(lambda), clip_re)
@@ -53,12 +54,16 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
                                   float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar, int method,
                                   double clip_re, double dt_scale) {
     const int p = blockIdx.x;
-    __shared__ double s_f[5];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2)
+    __shared__ double s_f[7];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2), 1/lambda
     __shared__ double s_gain[2];
-    // Only the first lane of each of the first four warps needs Delta and z:
+    // Only the first lane of each of the first five warps needs Delta and z:
     // float64 work on the other lanes would still occupy the SM's few float64
     // units, so they skip it.
-    const bool leader = (threadIdx.x & 31) == 0 && threadIdx.x < 128;
+    const bool leader = (threadIdx.x & 31) == 0 && threadIdx.x < 160;
+    // this thread's first B_tilde element, fetched now so that its latency
+    // overlaps the float64 work below
+    const float2 *src = b_tilde + (size_t)p * H;
+    const float2 bt0 = (int)threadIdx.x < H ? src[threadIdx.x] : make_float2(0.f, 0.f);
     dcplx lam = {0.0, 0.0}, z = {0.0, 0.0};
     double dt = 0.0;
     if (leader) {
@@ -83,6 +88,12 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
         else if (w == 1) s_f[2] = exp(z.re);
         else if (w == 2) s_f[3] = expm1(z.re);
         else if (w == 3) s_f[4] = sin(0.5 * z.im);
+        else if (w == 4) {
+            // 1/lambda, off the path of the functions above
+            const double den = lam.re * lam.re + lam.im * lam.im;
+            s_f[5] = lam.re / den;
+            s_f[6] = -lam.im / den;
+        }
     }
     __syncthreads();
     if (method != 1 && threadIdx.x == 0) {
@@ -103,7 +114,7 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
             gain = {dt * phi.re, dt * phi.im};
         } else {
             const dcplx em1 = {em1r * c - 2.0 * sh * sh, mag * s};
-            gain = ddiv(em1, lam);
+            gain = dmul(em1, dcplx{s_f[5], s_f[6]});
         }
         lambda_bar[p] = make_float2((float)(mag * c), (float)(mag * s));
         s_gain[0] = gain.re;
@@ -111,10 +122,9 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
     }
     __syncthreads();
     const dcplx g = {s_gain[0], s_gain[1]};
-    const float2 *src = b_tilde + (size_t)p * H;
     float2 *dst = b_bar + (size_t)p * H;
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        const float2 bt = src[h];
+        const float2 bt = h == (int)threadIdx.x ? bt0 : src[h];
         const dcplx v = dmul(g, dcplx{(double)bt.x, (double)bt.y});
         dst[h] = make_float2((float)v.re, (float)v.im);
     }
@@ -145,7 +155,7 @@ __global__ void mode_consts_kernel(const float2 *__restrict__ lambda, const floa
 cudaError_t launch_discretize(const float2 *lambda, const float *log_dt, const float2 *b_tilde,
                               int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st, int method,
                               double clip_re, double dt_scale) {
-    const int threads = H >= 256 ? 256 : 128;   // at least four warps (see discretize_kernel)
+    const int threads = H >= 256 ? 256 : 160;   // at least five warps (see discretize_kernel)
     discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar, method, clip_re,
                                              dt_scale);
     return cudaGetLastError();
