@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(SIMT_THREADS)
 fwd_simt_kernel(const SimtArgs args) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ long long s_tile;
-    __shared__ unsigned s_flag, s_epoch, s_drop, s_bad;
+    __shared__ unsigned s_epoch, s_drop, s_bad;
+    __shared__ unsigned s_st[32];   // look-back window: status of predecessors c-1, c-2, ...
+    __shared__ int s_n, s_stop;
     __shared__ unsigned long long s_limit;
 
     const int tid = threadIdx.x;
@@ -264,25 +266,58 @@ fwd_simt_kernel(const SimtArgs args) {
                 __threadfence();
                 st_release(args.ws.flags + tile, (epoch << 2) | FLAG_AGG);
             }
-            for (int j = c - 1;; --j) {
-                const long long jt = (long long)j * B + b;
-                if (tid == 0) s_flag = wait_flag(hdr, args.ws.flags + jt, epoch, s_limit, (unsigned)tile);
+            // Warp-wide look-back: lane l of warp 0 waits for predecessor
+            // chunk jn - l (nearest first) to publish at least its aggregate;
+            // a ballot finds the nearest one that is inclusive (or gave up).
+            // The block then folds that whole window at once, nearest first,
+            // and moves 32 chunks back only if every one was an aggregate.
+            for (int jn = c - 1;; jn -= 32) {
+                if (tid < 32) {
+                    const int j = jn - tid;
+                    unsigned st = 0;
+                    if (j >= 0) st = wait_flag(hdr, args.ws.flags + (long long)j * B + b, epoch, s_limit, (unsigned)tile);
+                    const unsigned stop = __ballot_sync(0xffffffffu, j < 0 || st != FLAG_AGG);
+                    s_st[tid] = st;
+                    if (tid == 0) {
+                        s_n = stop ? __ffs(stop) : 32;
+                        s_stop = stop != 0;
+                    }
+                }
                 __syncthreads();
-                const unsigned st = s_flag;
+                const int n = s_n;
                 for (int p = tid; p < P; p += SIMT_THREADS) {
                     float4 cs = carry_s[p];
                     float2 mult = make_float2(cs.x, cs.y), accv = make_float2(cs.z, cs.w);
-                    if (st == FLAG_AGG) {
-                        const float4 v = __ldcg(args.ws.agg + jt * P + p);
-                        accv = cfma(mult, make_float2(v.z, v.w), accv);
-                        mult = cmul(mult, make_float2(v.x, v.y));
-                    } else if (st == FLAG_INCL) {
-                        accv = cfma(mult, __ldcg(args.ws.incl + jt * P + p), accv);
+                    for (int l0 = 0; l0 < n; l0 += 8) {
+                        float4 v[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int l = l0 + q;
+                            v[q] = make_float4(1.f, 0.f, 0.f, 0.f);
+                            if (l < n) {
+                                const long long jt = (long long)(jn - l) * B + b;
+                                if (s_st[l] == FLAG_AGG) {
+                                    v[q] = __ldcg(args.ws.agg + jt * P + p);
+                                } else if (s_st[l] == FLAG_INCL) {
+                                    const float2 inc = __ldcg(args.ws.incl + jt * P + p);
+                                    v[q] = make_float4(0.f, 0.f, inc.x, inc.y);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int l = l0 + q;
+                            if (l < n && (s_st[l] == FLAG_AGG || s_st[l] == FLAG_INCL)) {
+                                // aggregate (A, E): acc += mult E, mult *= A; inclusive: acc += mult x
+                                accv = cfma(mult, make_float2(v[q].z, v[q].w), accv);
+                                mult = cmul(mult, make_float2(v[q].x, v[q].y));
+                            }
+                        }
                     }
                     carry_s[p] = make_float4(mult.x, mult.y, accv.x, accv.y);
                 }
                 __syncthreads();
-                if (st != FLAG_AGG) break;
+                if (s_stop) break;
             }
         }
         for (int p = tid; p < P; p += SIMT_THREADS) {

@@ -136,7 +136,7 @@ __device__ inline unsigned wait_flag(WsHeader *hdr, const unsigned int *f, unsig
             return 0;
         }
         __nanosleep(backoff);
-        if (backoff < 1024) backoff <<= 1;
+        if (backoff < 128) backoff <<= 1;
     }
 }
 
