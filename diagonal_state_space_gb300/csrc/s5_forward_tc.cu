@@ -17,22 +17,22 @@
 // on in registers.
 //
 // Each CTA runs a warp-specialised pipeline over its tiles:
-//   warps 0-3   TMA and tcgen05.mma issue (one thread each):
-//                 TMA: u tile [64 tokens x 128 features] bf16 -> smem (4
-//                 stages, freed as soon as GEMM1 has read it); bulk copy of
-//                 the two weight images at start-up
-//                 GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T      (into TMEM)
-//                 GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T      (into TMEM)
-//               Each GEMM is split over two threads (rows / k-steps), so that
-//               four chains of dependent MMAs are in flight.  Warp 2 also
-//               allocates TMEM (512 columns: 4 regions of 128).
+//   warp 0      TMA: u tile [64 tokens x 128 features] bf16 -> smem (3 stages,
+//               freed once GEMM1 has read it); bulk copy of the two weight
+//               images at start-up
+//   warp 1      GEMM1  Bu^T[2P x 64] = Bs[2P x H] * u^T  (16 MMAs from one
+//               thread into the tile's TMEM region: Re rows, then Im rows)
+//   warp 2      GEMM2  y^T [H  x 64] = C'[H x 2P] * X^T  (16 MMAs from one
+//               thread into columns 0..63 of the region, once X is complete);
+//               TMEM allocation (512 columns: 4 regions of 128)
+//   warp 3      a second TMA copy of each tile's u, for the epilogue
 //   warps 4-7   scan, thread = mode = TMEM lane, pass 1 two tiles ahead: pass 1
-//               of tile i+2 (end state from zero, published as the tile's
-//               aggregate record), then pass 2 of tile i from its carry (two
-//               interleaved 32-step chains), written as bf16 into the GEMM2
-//               operand X [64 x 2P]
+//               of tile i+2 (four 16-token chains from zero; the tile's end
+//               state is published as its aggregate record), then pass 2 of
+//               tile i (the four chains from the carry), written as bf16 into
+//               the GEMM2 operand X [64 x 2P]
 //   warps 8-11  epilogue, thread = feature = TMEM lane of GEMM2:
-//               y = D2 + D*u (u re-read through L2), bf16 stores
+//               y = acc + D*u (u from the shared copy), bf16 stores
 //   warps 12-15 carries, thread = mode: wait for the tile's carry record and
 //               put it into a shared-memory slot (two slots), ahead of the scan.
 // The scanner CTAs run none of this: threads 0..P-1 only.
