@@ -71,3 +71,34 @@ def test_host_validation_needs_no_gpu(lib):
              fake, 1 << 30, None]
     assert lib.s5_forward_varying_dt(*vargs) == INV    # dt_scale missing
     assert lib.s5_sync_status(None, None) == INV
+
+
+def test_host_validation_of_the_next_row_entry_points(lib):
+    INV, OK = 1, 0
+    fake = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced on these paths
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    f = ctypes.c_float
+    # discretisation options: unknown method, non-positive rate factor, positive clip
+    ok_args = [fake, fake, fake, 4, 4, 0, f(0.0), f(1.0), fake, fake, None]
+    for i, v in ((5, 2), (7, f(0.0)), (7, f(-1.0)), (6, f(1e-4)), (3, 0)):
+        bad = list(ok_args); bad[i] = v
+        assert lib.s5_discretize_ex(*bad) == INV
+    bad = list(ok_args); bad[1] = mis
+    assert lib.s5_discretize_ex(*bad) == INV
+    # streaming step: bad sizes and parameters are rejected; an empty batch is a no-op
+    assert lib.s5_step(fake, fake, fake, fake, fake, fake, fake, -1, 8, 4, None) == INV
+    assert lib.s5_step(None, fake, fake, fake, fake, fake, fake, 1, 8, 4, None) == INV
+    assert lib.s5_step(fake, fake, fake, fake, fake, fake, fake, 1, 0, 4, None) == INV
+    assert lib.s5_step(fake, fake, fake, fake, None, None, None, 0, 8, 4, None) == OK
+    # bidirectional layer
+    assert lib.s5_bidirectional_workspace_size(-1, 1, 1, 1, 0, 0) == 0
+    assert lib.s5_bidirectional_workspace_size(1, 1, 1, 1, 9, 0) == 0
+    n1 = lib.s5_bidirectional_workspace_size(2, 100, 8, 4, 0, 0)
+    assert n1 >= lib.s5_workspace_size(2, 100, 8, 4)
+    bargs = [fake, fake, fake, fake, fake, 0, fake, 0, 0, 2, 100, 8, 4, fake, n1, None]
+    bad = list(bargs); bad[2] = None                   # no c_tilde2
+    assert lib.s5_forward_bidirectional(*bad) == INV
+    bad = list(bargs); bad[14] = 16                    # workspace too small
+    assert lib.s5_forward_bidirectional(*bad) == INV
+    bad = list(bargs); bad[10] = 0                     # L = 0: nothing to do
+    assert lib.s5_forward_bidirectional(*bad) == OK
