@@ -54,6 +54,9 @@ __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float
                                   float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar, int method,
                                   double clip_re, double dt_scale) {
     const int p = blockIdx.x;
+    // the kernel that consumes Lambda_bar and B_bar may be scheduled now; it
+    // waits for this one to complete before reading them
+    griddep_launch_dependents();
     __shared__ double s_f[7];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2), 1/lambda
     __shared__ double s_gain[2];
     // Only the first lane of each of the first five warps needs Delta and z:

@@ -511,6 +511,11 @@ __device__ __forceinline__ bool scan_front(ScanTile &T, int i, const Lane &ln, i
 // ---------------------------------------------------------------------------
 __global__ void weight_images_kernel(const float2 *__restrict__ b_bar, const float2 *__restrict__ c_tilde,
                                      unsigned char *__restrict__ img) {
+    // launched programmatically: the scan kernel after it may be scheduled
+    // at once; B_bar and C~ are read, and the images written, only after the
+    // previous kernel (which may produce the former or read the latter) ends
+    griddep_launch_dependents();
+    griddep_wait();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx < P_M * H_F / 2) {
         // Bs: rows 0..P-1 = Re B_bar, rows P..2P-1 = Im B_bar, K = H
@@ -560,6 +565,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
 
     if (fits && scanner) {
         // ------------------------------------------------------------ sequence scanner
+        griddep_wait();
         if (threadIdx.x < P_M) {
             const int m = threadIdx.x, b = ln.k - B * W;
             const unsigned ep = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
@@ -593,6 +599,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             }
             sb->abort = 0;
             fence_mbar_init();
+            griddep_wait();
             sb->epoch = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
             sb->drop = *reinterpret_cast<volatile unsigned *>(&hdr->drop_publish);
             const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
@@ -603,8 +610,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             tmem_relinquish();
         }
     } else if (threadIdx.x == 0) {
+        griddep_wait();
         latch_status(hdr, S5_ERR_UNSUPPORTED);
     }
+    // barrier set-up and the TMEM allocation above overlap the end of the
+    // kernel before this one; nothing global is touched before this wait
+    griddep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -924,6 +935,20 @@ bool make_map(CUtensorMap *map, const void *base, int B, int L) {
     return r == CUDA_SUCCESS;
 }
 
+// The bf16 images of B_bar and C' that the scan kernel bulk-copies in.
+cudaError_t launch_weight_images(const TcArgs &a, cudaStream_t st) {
+    const int words = P_M * H_F / 2 + H_F * P_M;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((words + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    set_programmatic(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, weight_images_kernel, a.b_bar, a.c_tilde, a.ws.wimg);
+}
+
 }  // namespace
 
 #if !S5_TC_REV
@@ -954,9 +979,7 @@ cudaError_t launch_forward_tc(const TcArgs &a0, const void *u, cudaStream_t st, 
     tc_grid(a.B, a.nchunks, num_sms, &a.W, &G);
     CUtensorMap mu;
     if (!make_map(&mu, u, a.B, a.L)) return cudaErrorInvalidValue;
-    const int words = P_M * H_F / 2 + H_F * P_M;
-    weight_images_kernel<<<(words + 255) / 256, 256, 0, st>>>(a.b_bar, a.c_tilde, a.ws.wimg);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_weight_images(a, st);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_REQUEST);
@@ -972,11 +995,12 @@ cudaError_t launch_forward_tc(const TcArgs &a0, const void *u, cudaStream_t st, 
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_REQUEST;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    set_programmatic(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fwd_tc_kernel, mu, a);
 }
 
@@ -991,9 +1015,7 @@ cudaError_t launch_backward_add_tc(const TcArgs &a0, const void *u, cudaStream_t
     CUtensorMap mu, my;
     if (!make_map(&mu, u, a.B, a.L)) return cudaErrorInvalidValue;
     if (!make_map(&my, a.y, a.B, a.L)) return cudaErrorInvalidValue;
-    const int words = P_M * H_F / 2 + H_F * P_M;
-    weight_images_kernel<<<(words + 255) / 256, 256, 0, st>>>(a.b_bar, a.c_tilde, a.ws.wimg);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_weight_images(a, st);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_REQUEST);
     if (e != cudaSuccess) return e;
@@ -1007,11 +1029,12 @@ cudaError_t launch_backward_add_tc(const TcArgs &a0, const void *u, cudaStream_t
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_REQUEST;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    set_programmatic(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, bwd_tc_kernel, mu, my, a);
 }
 #endif

@@ -102,6 +102,23 @@ __device__ __forceinline__ void latch_status(WsHeader *h, unsigned code) {
     atomicCAS(&h->status, 0u, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may be scheduled while the kernel before it
+// in the stream is still running; griddep_wait() returns once that kernel
+// has completed and its writes are visible, so every read or write of memory
+// the previous kernel may touch comes after it.  In a kernel launched without
+// the attribute it returns at once.  griddep_launch_dependents() lets the
+// next such kernel be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline void set_programmatic(cudaLaunchAttribute &a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+}
+
 __device__ __forceinline__ unsigned ld_acquire(const unsigned int *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

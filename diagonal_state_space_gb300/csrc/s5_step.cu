@@ -74,6 +74,11 @@ step_cluster_kernel(const float2 *__restrict__ lambda_bar, const float2 *__restr
     float2 *sx_all = sx_own + STEP_SEQ * mp;                 // [STEP_SEQ][P]: every mode's new state
     float *su = reinterpret_cast<float *>(sx_all + STEP_SEQ * P);   // [STEP_SEQ][H]
 
+    // nothing is read before the previous kernel in the stream (the step
+    // before, which writes x) ends; then the next step may be scheduled
+    griddep_wait();
+    griddep_launch_dependents();
+
     // everything the first mode and feature of this warp need, fetched at once
     const int pf = p0 + warp, hf = h0 + warp;
     float2 bw[STEP_KC], cw[STEP_KC];
@@ -264,13 +269,14 @@ cudaError_t launch_step(const float2 *lambda_bar, const float2 *b_bar, const flo
     cfg.blockDim = dim3(STEP_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = STEP_CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_programmatic(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, step_cluster_kernel, lambda_bar, b_bar, c_tilde, d, x, u, y, B, H, P);
 }
 
