@@ -67,6 +67,43 @@ def test_tc_repeat_calls_share_a_workspace():
     assert rel_l2(outs[1], outs[2]) <= 1e-3
 
 
+def test_tc_back_to_back_layers_match_synchronised_calls():
+    """Two layers on one stream with no host synchronisation: the second
+    layer's discretisation runs between the forwards and its forward reads
+    the first one's output.  The kernels of the path may be scheduled while
+    the kernel before them finishes, so each must wait for that kernel before
+    touching its results; the chain must give what the same calls give with
+    the device synchronised after every call.  A kernel that read another
+    layer's weights or an unfinished input would differ by O(1)."""
+    B, L = 8, 4097
+    inp1 = make_layer_inputs(B, L, 128, 128, seed=41, u_dtype="bf16")
+    inp2 = make_layer_inputs(B, L, 128, 128, seed=42, u_dtype="bf16")
+    t1, t2 = layer_to_device(inp1, "bf16"), layer_to_device(inp2, "bf16")
+
+    def two_layers(sync):
+        def barrier():
+            if sync:
+                torch.cuda.synchronize()
+        lb1, bb1 = api.s5_discretize(t1["lam"], t1["log_dt"], t1["b_tilde"])
+        barrier()
+        y1 = api.s5_forward(lb1, bb1, t1["c_tilde"], t1["d"], t1["u"], proj_dtype="bf16")
+        barrier()
+        lb2, bb2 = api.s5_discretize(t2["lam"], t2["log_dt"], t2["b_tilde"])
+        barrier()
+        y2 = api.s5_forward(lb2, bb2, t2["c_tilde"], t2["d"], y1, proj_dtype="bf16")
+        torch.cuda.synchronize()
+        return host(y1), host(y2)
+
+    torch.cuda.synchronize()
+    for _ in range(2):
+        c1, c2 = two_layers(sync=False)
+        s1, s2 = two_layers(sync=True)
+        assert rel_l2(c1, s1) <= 1e-3
+        assert rel_l2(c2, s2) <= 1e-3
+    oy1, _ = oracle_forward(inp1)
+    assert rel_l2(c1, oy1) <= BF16_TOL
+
+
 def test_tc_carry_wait_timeout_is_reported_and_recoverable():
     inp = make_layer_inputs(1, 1024, 128, 128, seed=4, u_dtype="bf16")
     t = layer_to_device(inp, "bf16")
