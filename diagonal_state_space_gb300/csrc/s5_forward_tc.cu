@@ -71,7 +71,7 @@ constexpr int P_M = 128;                // stored complex modes
 constexpr int STAGES = 3;
 constexpr int REGIONS = 4;              // TMEM regions of 128 columns
 constexpr int THREADS = 512;
-constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;   // warp 3 is idle
+constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;   // warp 3: the epilogue's u copy
 constexpr int W_MAX = 64;               // lanes per sequence at most
 constexpr int RB = 18;                  // aggregate records loaded per round
 constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps

@@ -24,6 +24,12 @@
  *    launch errors.  Conditions only the GPU can see (a non-finite or
  *    negative interval, a carry wait that gave up) are latched in the
  *    workspace and reported by s5_sync_status().
+ *  - Stream order is kept.  Some kernels (the weight images and scans of
+ *    s5_forward and s5_forward_bidirectional on the tensor-core shapes, and
+ *    s5_step) are launched with programmatic dependent launch: they may be
+ *    scheduled while the kernel queued before them is still running, but
+ *    each waits for that kernel to complete before it reads or writes any
+ *    memory.
  *  - No CPU fallback exists: a shape the kernels do not cover returns
  *    S5_ERR_UNSUPPORTED.
  */
