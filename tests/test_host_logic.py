@@ -1,6 +1,8 @@
 """Host-side logic that needs no GPU: the seeded input generators' options and
 the benchmark's argument defaults."""
+import json
 import os
+import subprocess
 import sys
 
 import numpy as np
@@ -66,3 +68,71 @@ def test_algorithmic_bytes_of_the_long_sequence_workload():
     assert bench.algorithmic_bytes(w, 2, 2) == expect == 67372544
     wb = WORKLOADS["pathx_bf16_bidir"]
     assert bench.algorithmic_bytes(wb, 2, 2) == expect + 8 * 128 * 128
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the float64 oracle on the host: no GPU is involved
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "small", "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["value"] == d["cpu_baseline"]["value"] == d["e2e"]["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # one sequence of the workload per step, timed as tokens per second
+    w = WORKLOADS["small"]
+    assert abs(d["value"] - w.L / (d["ms_per_step"] / 1e3)) <= 1e-6 * d["value"]
+
+
+class _DoneProcess:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_sampler_takes_the_median_and_the_throttle_reasons():
+    import bench
+
+    s = bench.ClockSampler(None)
+    s.proc = _DoneProcess()
+    # index, sm, max sm, power, active, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap
+    s.out.write("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+                "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                "0, [N/A], 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    c = s.stop()
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"]
+    s = bench.ClockSampler(None)
+    s.proc = _DoneProcess()
+    s.out.write("0, 1500, 2070, 700.0, 0x48, Active, Not Active, Active, Not Active\n")
+    assert s.stop()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_traffic_is_reported_only_for_the_captured_source_and_workload(tmp_path, monkeypatch):
+    import hashlib
+
+    import bench
+
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel source\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(
+        {"k": {"workload": "pathx_bf16 (B=8 ...)", "source_sha256": sha, "dram_bytes_per_launch": 1234}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("k", str(src), "pathx_bf16") == 1234.0
+    assert bench.traffic_for("k", str(src), "fp32") is None          # another workload
+    assert bench.traffic_for("other", str(src), "pathx_bf16") is None
+    src.write_text("// kernel source, edited\n")                     # changed since the capture
+    assert bench.traffic_for("k", str(src), "pathx_bf16") is None
