@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
+from _golden import read_golden
 from diagonal_state_space_gb300 import init as s5init
 
 scipy_integrate = pytest.importorskip("scipy.integrate")
@@ -152,7 +153,7 @@ def test_bidirectional_equals_explicit_sums():
 
 
 # --------------------------------------------------------------------------
-# HiPPO-N (review row 5; summary App. B.1.1; S4 page "Diagonal plus low-rank").
+# HiPPO-N (review row 5; summary App. B.1.1; S4 page "Normal plus low-rank").
 # --------------------------------------------------------------------------
 def test_hippo_normal_structure_and_the_eigenvalues_printed_at_n8():
     a = s5init.hippo_normal(8)
@@ -166,11 +167,13 @@ def test_hippo_normal_structure_and_the_eigenvalues_printed_at_n8():
     legs = -np.tril(np.sqrt(np.outer(2 * n + 1, 2 * n + 1)), -1) - np.diag(n + 1.0)
     pp = 0.5 * np.outer(np.sqrt(2 * n + 1), np.sqrt(2 * n + 1))
     assert np.allclose(legs + pp, a, rtol=0, atol=1e-14)
+    g = read_golden("hippo_n_n8_eigenvalues.txt")
+    assert int(g["n"][0]) == 8
     ev, v = s5init.hippo_normal_eig(8)
-    assert np.allclose(ev.real, -0.5, atol=1e-12)
-    printed = np.array([19.857, 5.354, 1.958, 0.427])
+    assert np.allclose(ev.real, float(g["real_part"][0]), atol=1e-12)
+    printed = np.array([float(x) for x in g["imag_abs_descending"]])
     got = np.sort(np.abs(ev.imag))[::-1][::2]
-    assert np.allclose(np.round(got, 3), printed, atol=0)
+    assert np.allclose(np.round(got, int(g["decimals"][0])), printed, atol=0)
     assert np.allclose(v @ np.diag(ev) @ v.conj().T, a, atol=1e-12)
     assert np.allclose(np.linalg.eigvals(a).real, -0.5, atol=1e-9)
 

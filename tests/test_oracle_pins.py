@@ -6,7 +6,6 @@ linear filter (scipy.signal.lfilter), an ODE integrator (scipy solve_ivp),
 closed forms, the worked example printed on the S4 page, finite differences,
 and PyTorch's own LayerNorm / GELU / sigmoid routines.
 """
-import os
 from fractions import Fraction
 from functools import lru_cache
 
@@ -14,11 +13,11 @@ import numpy as np
 import pytest
 
 import oracle
+from _golden import read_golden
 
 scipy_signal = pytest.importorskip("scipy.signal")
 scipy_integrate = pytest.importorskip("scipy.integrate")
 
-GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _rng(seed):
@@ -157,15 +156,6 @@ def test_impulse_response_is_convolution_kernel():
         np.testing.assert_allclose(y[0], expect, rtol=1e-12, atol=1e-12)
 
 
-def _read_golden(name):
-    out = {}
-    with open(os.path.join(GOLDEN, name)) as f:
-        for line in f:
-            if line.startswith("#") or not line.strip():
-                continue
-            k, v = line.split(":", 1)
-            out[k.strip()] = v.split()
-    return out
 
 
 def test_s4_page_worked_example_scalar_pulse():
@@ -173,7 +163,7 @@ def test_s4_page_worked_example_scalar_pulse():
     (2/3)(1/3)^i, pulse (1,1,1,1,0,0,0,0).  Reached through the zero-order hold
     with a real pole lambda = -ln 3, interval 1 and B~ = ln 3 (so lambda_bar = 1/3
     and B_bar = 2/3), and C~ = 1/2 so that the factor-2 readout reads x itself."""
-    g = _read_golden("s4_scalar_pulse.txt")
+    g = read_golden("s4_scalar_pulse.txt")
     pulse = [int(v) for v in g["pulse"]]
     kern = [Fraction(int(n), int(dn)) for n, dn in zip(g["kernel_num"], g["kernel_den"])]
     L = len(pulse)
