@@ -22,14 +22,18 @@ def _rng(seed):
 
 
 # --------------------------------------------------------------------------
-# Bilinear transform (S4 page, "Discretize": lambda = -64 at Delta = 0.1 goes
-# to (1 - 3.2)/(1 + 3.2) = -0.524, lambda = -1 to 0.9048).
+# Bilinear transform (S4 page, "Discretization and the step size Δ": two real
+# eigenvalues at Delta = 0.1 and the values the page gives for their images,
+# kept with the citation in tests/golden/s4_bilinear_examples.txt).
 # --------------------------------------------------------------------------
 def test_bilinear_matches_the_values_printed_on_the_s4_page():
-    lam = np.array([-64.0 + 0j, -1.0 + 0j])
-    lb, bb = oracle.discretize_ex(lam, np.log([0.1, 0.1]), np.ones((2, 1)), method="bilinear")
-    assert round(lb[0].real, 3) == -0.524 and abs(lb[0].imag) == 0.0
-    assert round(lb[1].real, 4) == 0.9048
+    g = read_golden("s4_bilinear_examples.txt")
+    lam = np.array([float(v) for v in g["lambda"]], dtype=np.complex128)
+    step = float(g["step"][0])
+    lb, bb = oracle.discretize_ex(lam, np.log(np.full(lam.size, step)), np.ones((lam.size, 1)),
+                                  method="bilinear")
+    for got, printed, nd in zip(lb, g["lambda_bar_bilinear"], g["printed_decimals"]):
+        assert round(got.real, int(nd)) == float(printed) and abs(got.imag) == 0.0
     # the stable region: every Re(lambda) < 0 maps into the open unit disk (the page's claim)
     rng = _rng(1)
     lam = -rng.uniform(1e-3, 100, 200) + 1j * rng.uniform(-100, 100, 200)
