@@ -14,7 +14,7 @@ import torch
 from diagonal_state_space_gb300 import api
 from diagonal_state_space_gb300 import init as s5init
 from diagonal_state_space_gb300._native import S5Error
-from diagonal_state_space_gb300.workloads import bf16_round, make_layer_inputs
+from diagonal_state_space_gb300.workloads import WORKLOADS, bf16_round, make_inputs, make_layer_inputs
 
 from _parity import dev, host, layer_to_device, rel_l2
 import oracle
@@ -85,7 +85,7 @@ def test_step_matches_oracle(B, H, P, steps):
     for k in range(steps):
         uk = np.ascontiguousarray(inp["u"][:, k])
         y = api.s5_step(lb, bb, t["c_tilde"], t["d"], x, dev(uk))
-        ox, oy = oracle.step(host(lb), host(bb), inp["c_tilde"], inp["d"], ox, uk)
+        ox, oy = oracle.step(olb, obb, inp["c_tilde"], inp["d"], ox, uk)
         assert rel_l2(host(y), oy) <= FP32_TOL
         # the D*u-free part alone
         assert rel_l2(host(y) - inp["d"] * uk, oy - inp["d"] * uk) <= FP32_TOL
@@ -161,10 +161,11 @@ def test_bidirectional_f32_matches_oracle(B, L, H, P):
     c2 = _c2(inp, L)
     t = layer_to_device(inp)
     lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
     for dz in (False, True):
         d = np.zeros_like(inp["d"]) if dz else inp["d"]
         y = api.s5_forward_bidirectional(lb, bb, dev(c2), dev(d), t["u"])
-        oy = oracle.forward_bidirectional(host(lb), host(bb), c2, d, inp["u"])
+        oy = oracle.forward_bidirectional(olb, obb, c2, d, inp["u"])
         assert rel_l2(host(y), oy) <= FP32_TOL, (dz, rel_l2(host(y), oy))
 
 
@@ -179,11 +180,12 @@ def test_bidirectional_bf16_tensor_core_path_matches_oracle(B, L):
     lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
     y = api.s5_forward_bidirectional(lb, bb, dev(c2), t["d"], t["u"], proj_dtype="bf16")
     assert y.dtype == torch.bfloat16
-    oy = oracle.forward_bidirectional(host(lb), host(bb), c2, inp["d"], inp["u"])
+    olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    oy = oracle.forward_bidirectional(olb, obb, c2, inp["d"], inp["u"])
     assert rel_l2(host(y.float()), oy) <= BF16_TOL
     # the SSM terms alone (D = 0)
     y0 = api.s5_forward_bidirectional(lb, bb, dev(c2), dev(np.zeros(H, np.float32)), t["u"], proj_dtype="bf16")
-    oy0 = oracle.forward_bidirectional(host(lb), host(bb), c2, np.zeros(H), inp["u"])
+    oy0 = oracle.forward_bidirectional(olb, obb, c2, np.zeros(H), inp["u"])
     assert rel_l2(host(y0.float()), oy0) <= BF16_TOL
 
 
@@ -211,3 +213,54 @@ def test_forward_from_hippo_init_matches_oracle():
     olb, obb = oracle.discretize(lam, log_dt, bt)
     oy, _ = oracle.forward(olb, obb, ct, d, u)
     assert rel_l2(host(y), oy) <= FP32_TOL
+
+
+# --------------------------------------------------------------------------
+# The three NEXT-row benchmark workloads at full size, through the calls the
+# benchmark times; the oracle computes the first and last sequence (all eight
+# for the streaming workload, whose sequences are short).
+# --------------------------------------------------------------------------
+def test_full_size_bidirectional_workload_sampled():
+    w = WORKLOADS["pathx_bf16_bidir"]
+    inp = make_inputs(w)
+    t = layer_to_device(inp, w.u_dtype)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    y = api.s5_forward_bidirectional(lb, bb, dev(inp["c_tilde2"]), t["d"], t["u"], proj_dtype="bf16")
+    seqs = [0, w.B - 1]
+    olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    oy = oracle.forward_bidirectional(olb, obb, inp["c_tilde2"], inp["d"], inp["u"][seqs])
+    assert rel_l2(host(y.float())[seqs], oy) <= BF16_TOL
+    # the SSM terms alone
+    yd = host(y.float())[seqs] - inp["d"] * inp["u"][seqs].astype(np.float64)
+    assert rel_l2(yd, oy - inp["d"] * inp["u"][seqs].astype(np.float64)) <= BF16_TOL
+
+
+def test_full_size_bilinear_workload_sampled():
+    w = WORKLOADS["pathx_bf16_bilinear"]
+    inp = make_inputs(w)
+    t = layer_to_device(inp, w.u_dtype)
+    lb, bb = api.s5_discretize_ex(t["lam"], t["log_dt"], t["b_tilde"], method=w.method, clip_re=w.clip_re,
+                                  dt_scale=w.dt_scale)
+    y, xl = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16", x_last=True)
+    seqs = [0, w.B - 1]
+    olb, obb = oracle.discretize_ex(inp["lambda_"], inp["log_dt"], inp["b_tilde"], w.method,
+                                    float(np.float32(w.clip_re)), float(np.float32(w.dt_scale)))
+    oy, oxl = oracle.forward(olb, obb, inp["c_tilde"], inp["d"], inp["u"][seqs])
+    assert rel_l2(host(y.float())[seqs], oy) <= BF16_TOL
+    assert rel_l2(host(xl)[seqs], oxl) <= BF16_TOL
+
+
+def test_full_size_streaming_workload():
+    w = WORKLOADS["stream"]
+    inp = make_inputs(w)
+    t = layer_to_device(inp)
+    lb, bb = api.s5_discretize(t["lam"], t["log_dt"], t["b_tilde"])
+    x = torch.zeros(w.B, w.P, dtype=torch.complex64, device="cuda")
+    u_t = t["u"].transpose(0, 1).contiguous()          # [L, B, H]: one contiguous slice per call
+    ys = [api.s5_step(lb, bb, t["c_tilde"], t["d"], x, u_t[k]) for k in range(w.L)]
+    y = torch.stack(ys, dim=1)
+    olb, obb = oracle.discretize(inp["lambda_"], inp["log_dt"], inp["b_tilde"])
+    oy, oxl = oracle.forward(olb, obb, inp["c_tilde"], inp["d"], inp["u"])
+    assert rel_l2(host(y), oy) <= FP32_TOL
+    assert rel_l2(host(y) - inp["d"] * inp["u"], oy - inp["d"] * inp["u"]) <= FP32_TOL
+    assert rel_l2(host(x), oxl) <= FP32_TOL
