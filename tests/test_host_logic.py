@@ -137,16 +137,3 @@ def test_traffic_is_reported_only_for_the_captured_source_and_workload(tmp_path,
     src.write_text("// kernel source, edited\n")                     # changed since the capture
     assert bench.traffic_for("k", str(src), "pathx_bf16") is None
 
-
-def test_tests_named_in_the_design_notes_exist():
-    import glob
-    import re
-
-    design = open(os.path.join(ROOT, "DESIGN.md"), encoding="utf-8").read()
-    cited = set(re.findall(r"`(test_[A-Za-z0-9_]+)\*?`", design))
-    assert cited
-    src = "".join(open(f, encoding="utf-8").read() for f in glob.glob(os.path.join(ROOT, "tests", "*.py")))
-    defined = set(re.findall(r"def (test_[A-Za-z0-9_]+)", src))
-    # a trailing * in the notes names a family of tests by prefix
-    missing = sorted(n for n in cited if not any(d == n or d.startswith(n) for d in defined))
-    assert not missing, missing
