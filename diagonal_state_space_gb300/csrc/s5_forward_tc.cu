@@ -71,7 +71,7 @@ constexpr int P_M = 128;                // stored complex modes
 constexpr int STAGES = 3;
 constexpr int REGIONS = 4;              // TMEM regions of 128 columns
 constexpr int THREADS = 512;
-constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;   // warp 3: the epilogue's u copy
+constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;
 constexpr int W_MAX = 64;               // lanes per sequence at most
 constexpr int RB = 18;                  // aggregate records loaded per round
 constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps
@@ -579,20 +579,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         if (threadIdx.x == 0) {
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(&sb->full_u[s], 1);
-                mbar_init(&sb->empty_u[s], 1);     // GEMM1's commit
+                mbar_init(&sb->empty_u[s], 2);     // the commits of GEMM1's two halves
             }
             for (int r = 0; r < REGIONS; ++r) {
-                mbar_init(&sb->tmem_full[r], 1);   // GEMM1's commit
+                mbar_init(&sb->tmem_full[r], 2);   // the commits of GEMM1's two halves
                 mbar_init(&sb->tmem_empty[r], 4);  // the four epilogue warps
                 mbar_init(&sb->p2read[r], 4);      // the four scan warps
-                mbar_init(&sb->mma2_done[r], 1);   // GEMM2's commit
+                mbar_init(&sb->mma2_done[r], 2);   // the commits of GEMM2's two halves
             }
             mbar_init(&sb->xready, 4);             // the four scan warps
-            mbar_init(&sb->xfree, 1);              // GEMM2's commit
+            mbar_init(&sb->xfree, 2);              // the commits of GEMM2's two halves
             mbar_init(&sb->eu_full, 1);
             mbar_init(&sb->eu_empty, 4);           // the four epilogue warps
             mbar_init(&sb->weights, 1);
-            mbar_init(&sb->drain, 2);          // the two MMA-issuing threads
+            mbar_init(&sb->drain, 4);          // the four MMA-issuing threads
             for (int q = 0; q < 2; ++q) {
                 mbar_init(&sb->carry_full[q], 4);    // the four fold warps
                 mbar_init(&sb->carry_empty[q], 4);   // the four scan warps
@@ -625,39 +625,36 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
 
     if (!pipeline) {
         // nothing to run: straight to the teardown
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ u for the epilogue
-        // A second TMA load of each tile's u, into the epilogue's buffer once
-        // the epilogue has read the previous tile's copy.
-        if (lane == 0) {
-            int last = -1;
-            for (int i = 0; i < n; ++i) {
-                if (i > 0 && !pipe_wait(&sb->eu_empty, (i - 1) & 1, sb, hdr)) break;
-                int b, c;
-                ln.tile(i, b, c);
-                mbar_arrive_tx(&sb->eu_full, U_STAGE);
-#if S5_TC_REV
-                c = nchunks - 1 - c;
-                tma_load_3d(smem + SM_EU, &tmap_e, 0, c * T_TOK, b, &sb->eu_full);
-                tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_e, 64, c * T_TOK, b, &sb->eu_full);
-#else
-                tma_load_3d(smem + SM_EU, &tmap_u, 0, c * T_TOK, b, &sb->eu_full);
-                tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->eu_full);
-#endif
-                last = i;
-            }
-            // the copy in flight must land before the CTA exits
-            if (last >= 0) drain_wait(&sb->eu_full, last & 1);
-        }
-    } else if (warp < 3) {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ TMA and MMA issue
-        // One thread each: warp 0 loads u tiles, warp 1 issues GEMM1, warp 2
-        // GEMM2.  A thread issues a chain of MMAs whose descriptors are
-        // compile-time offsets at close to the tensor pipe's rate.
+        // One thread in each of the four sub-partitions issues MMAs: warp 0
+        // loads the u tiles and issues GEMM1's Re half, warp 1 GEMM1's Im
+        // half, warps 2 and 3 the two K halves of GEMM2 (modes 0..63 and
+        // 64..127).  A tensor pipe fed by one issuing thread slows down when
+        // the FMA-bound warps of the same sub-partition compete for its issue
+        // slots; spread over four, the issue keeps up with the pipe.
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, T_TOK);
             const uint32_t bs = smem_addr(smem + SM_BS), cp = smem_addr(smem + SM_CP);
             const uint32_t xs = smem_addr(smem + SM_X);
+            int issued = 0;   // u tiles 0 .. issued-1 have been requested
+            // u tile il into stage il % STAGES once GEMM1 has read the tile before
+            auto load_u = [&](int il) -> bool {
+                const int s = il % STAGES;
+                if (il >= STAGES && !pipe_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1, sb, hdr)) return false;
+                int b, c;
+                ln.tile(il, b, c);
+#if S5_TC_REV
+                c = nchunks - 1 - c;
+#endif
+                unsigned char *dst = smem + SM_U + s * U_STAGE;
+                mbar_arrive_tx(&sb->full_u[s], U_STAGE);
+                tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
+                tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
+                issued = il + 1;
+                return true;
+            };
+            bool ok = true;
             if (warp == 0) {
                 prefetch_tmap(&tmap_u);
 #if S5_TC_REV
@@ -666,85 +663,75 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                 mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
                 bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
                 bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
-                int last_issue[STAGES];
-                for (int q = 0; q < STAGES; ++q) last_issue[q] = -1;
-                for (int il = 0; il < n; ++il) {
-                    const int s = il % STAGES;
-                    if (il >= STAGES && !pipe_wait(&sb->empty_u[s], ((il / STAGES) - 1) & 1, sb, hdr)) break;
-                    int b, c;
-                    ln.tile(il, b, c);
-#if S5_TC_REV
-                    c = nchunks - 1 - c;
-#endif
-                    unsigned char *dst = smem + SM_U + s * U_STAGE;
-                    mbar_arrive_tx(&sb->full_u[s], U_STAGE);
-                    tma_load_3d(dst, &tmap_u, 0, c * T_TOK, b, &sb->full_u[s]);
-                    tma_load_3d(dst + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->full_u[s]);
-                    last_issue[s] = il;
+                for (int il = 0; il < n && il < STAGES; ++il) load_u(il);
+            }
+            ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
+            if (warp < 2) {
+                // GEMM1 of tile g into region g % REGIONS: Re rows (warp 0)
+                // into columns 0..63, Im rows (warp 1) into 64..127.
+                const int mb = warp;
+                const uint64_t da = sw128_kmajor_desc(bs);
+                for (int g = 0; ok && g < n; ++g) {
+                    const int s = g % STAGES, r = g % REGIONS;
+                    ok = pipe_wait(&sb->full_u[s], (g / STAGES) & 1, sb, hdr) &&
+                         (g < REGIONS || pipe_wait(&sb->tmem_empty[r], ((g / REGIONS) - 1) & 1, sb, hdr));
+                    if (!ok) break;
+                    tc_fence_after();
+                    // descriptors: a base plus compile-time offsets (a descriptor's
+                    // low bits hold the address / 16, and no offset carries out)
+                    const uint64_t db = sw128_kmajor_desc(smem_addr(smem + SM_U + s * U_STAGE));
+                    const uint64_t dam = da + (uint64_t)((mb * (P_M * 128)) >> 4);
+                    const uint32_t d0 = tmem + (uint32_t)r * 128u + (uint32_t)mb * 64u;
+#pragma unroll
+                    for (int kq = 0; kq < H_F / 16; ++kq) {
+                        const uint64_t a = dam + (uint64_t)(((kq >> 2) * (2 * P_M * 128) + (kq & 3) * 32) >> 4);
+                        const uint64_t bb = db + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
+                        if (kq == 0)
+                            mma_bf16_c<false>(d0, a, bb, idesc);
+                        else
+                            mma_bf16_c<true>(d0, a, bb, idesc);
+                    }
+                    mma_commit(&sb->tmem_full[r]);
+                    mma_commit(&sb->empty_u[s]);
+                    // warp 0 refills the stage tile g-1 used (its GEMM1 was
+                    // issued an iteration ago) with tile g-1+STAGES
+                    if (warp == 0 && g >= 1 && g - 1 + STAGES < n) ok = load_u(g - 1 + STAGES);
                 }
-                // copies still in flight must land before the CTA exits
-                drain_wait(&sb->weights, 0);
-                for (int q = 0; q < STAGES; ++q)
-                    if (last_issue[q] >= 0) drain_wait(&sb->full_u[q], (last_issue[q] / STAGES) & 1);
             } else {
-                bool ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
-                if (warp == 1) {
-                    // GEMM1 of tile g into region g % REGIONS: Re rows into
-                    // columns 0..63, Im rows into 64..127.
-                    const uint64_t da = sw128_kmajor_desc(bs);
-                    for (int g = 0; ok && g < n; ++g) {
-                        const int s = g % STAGES, r = g % REGIONS;
-                        ok = pipe_wait(&sb->full_u[s], (g / STAGES) & 1, sb, hdr) &&
-                             (g < REGIONS || pipe_wait(&sb->tmem_empty[r], ((g / REGIONS) - 1) & 1, sb, hdr));
-                        if (!ok) break;
-                        tc_fence_after();
-                        // descriptors: a base plus compile-time offsets (a descriptor's
-                        // low bits hold the address / 16, and no offset carries out)
-                        const uint64_t db = sw128_kmajor_desc(smem_addr(smem + SM_U + s * U_STAGE));
-                        const uint32_t d0 = tmem + (uint32_t)r * 128u;
+                // GEMM2 of tile g once X is complete (the scan warps have also
+                // read the tile's Bu by then): warp 2 sums modes 0..63 into
+                // columns 0..63 of the tile's region, warp 3 modes 64..127
+                // into columns 64..127; the epilogue adds the two.
+                const int kh = warp - 2;
+                const uint64_t dc = sw128_kmajor_desc(cp), dx = sw128_kmajor_desc(xs);
+                for (int g = 0; ok && g < n; ++g) {
+                    const int r = g % REGIONS;
+                    ok = pipe_wait(&sb->xready, g & 1, sb, hdr);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)r * 128u + (uint32_t)kh * 64u;
 #pragma unroll
-                        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-                            for (int kq = 0; kq < H_F / 16; ++kq) {
-                                const uint64_t a = da + (uint64_t)(((kq >> 2) * (2 * P_M * 128) + mb * (P_M * 128) +
-                                                                    (kq & 3) * 32) >> 4);
-                                const uint64_t bb = db + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
-                                if (kq == 0)
-                                    mma_bf16_c<false>(d0 + (uint32_t)mb * 64u, a, bb, idesc);
-                                else
-                                    mma_bf16_c<true>(d0 + (uint32_t)mb * 64u, a, bb, idesc);
-                            }
-                        mma_commit(&sb->tmem_full[r]);
-                        mma_commit(&sb->empty_u[s]);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int kq = 8 * kh + kk;
+                        const uint64_t a = dc + (uint64_t)(((kq >> 2) * (H_F * 128) + (kq & 3) * 32) >> 4);
+                        const uint64_t bb = dx + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
+                        if (kk == 0)
+                            mma_bf16_c<false>(d, a, bb, idesc);
+                        else
+                            mma_bf16_c<true>(d, a, bb, idesc);
                     }
-                } else {
-                    const uint64_t dc = sw128_kmajor_desc(cp), dx = sw128_kmajor_desc(xs);
-                    // GEMM2 of tile g into columns 0..63 of its region once X
-                    // is complete (the scan warps have also read the tile's
-                    // Bu by then): 16 MMAs back to back, since every wait or
-                    // commit between them lets the tensor pipe drain.
-                    for (int g = 0; ok && g < n; ++g) {
-                        const int r = g % REGIONS;
-                        ok = pipe_wait(&sb->xready, g & 1, sb, hdr);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t d = tmem + (uint32_t)r * 128u;
-#pragma unroll
-                        for (int kq = 0; kq < 16; ++kq) {
-                            const uint64_t a = dc + (uint64_t)(((kq >> 2) * (H_F * 128) + (kq & 3) * 32) >> 4);
-                            const uint64_t bb = dx + (uint64_t)(((kq >> 2) * (T_TOK * 128) + (kq & 3) * 32) >> 4);
-                            if (kq == 0)
-                                mma_bf16_c<false>(d, a, bb, idesc);
-                            else
-                                mma_bf16_c<true>(d, a, bb, idesc);
-                        }
-                        mma_commit(&sb->xfree);
-                        mma_commit(&sb->mma2_done[r]);
-                    }
+                    mma_commit(&sb->xfree);
+                    mma_commit(&sb->mma2_done[r]);
                 }
-                // every MMA issued must complete before TMEM is freed
-                mma_commit(&sb->drain);
-                drain_wait(&sb->drain, 0);
+            }
+            // every MMA issued must complete before TMEM is freed
+            mma_commit(&sb->drain);
+            drain_wait(&sb->drain, 0);
+            // copies still in flight must land before the CTA exits
+            if (warp == 0) {
+                drain_wait(&sb->weights, 0);
+                for (int il = max(0, issued - STAGES); il < issued; ++il)
+                    drain_wait(&sb->full_u[il % STAGES], (il / STAGES) & 1);
             }
         }
     } else if (warp >= W_SCAN && warp < W_SCAN + 4) {
@@ -812,11 +799,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         }
     } else if (warp >= W_EPI && warp < W_EPI + 4) {
         // ------------------------------------------------------------ epilogue
-        // thread = feature h = TMEM lane of GEMM2: y = acc + D * u over the
-        // tile's tokens.  The tile's u is loaded before waiting for GEMM2 and
-        // left untouched until after the wait (no instruction depends on the
-        // loads before then), so their latency overlaps the wait; the region
-        // is released once its last column is in registers.
+        // thread = feature h = TMEM lane of GEMM2: y = acc_lo + acc_hi + D * u
+        // over the tile's tokens.  The tile's u is loaded before waiting for
+        // GEMM2 and left untouched until after the wait (no instruction
+        // depends on the loads before then), so their latency overlaps the
+        // wait; the region is released once its last column is in registers.
+        // Lane 0 of warp W_EPI keeps the u buffer filled: a second TMA load of
+        // each tile's u, issued once all four warps have read the previous one.
         const int qd = warp - W_EPI;
         const int h = 32 * qd + lane;
 #if S5_TC_REV
@@ -829,6 +818,23 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         // this feature's u for token t: row t, column h of the swizzled copy
         const unsigned char *eu = smem + SM_EU + (h >> 6) * (T_TOK * 128);
         const uint32_t hc = (uint32_t)(h & 63);
+        const bool copier = qd == 0 && lane == 0;
+        int eu_last = -1;
+        auto load_eu = [&](int i) {
+            int b, c;
+            ln.tile(i, b, c);
+            mbar_arrive_tx(&sb->eu_full, U_STAGE);
+#if S5_TC_REV
+            c = nchunks - 1 - c;
+            tma_load_3d(smem + SM_EU, &tmap_e, 0, c * T_TOK, b, &sb->eu_full);
+            tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_e, 64, c * T_TOK, b, &sb->eu_full);
+#else
+            tma_load_3d(smem + SM_EU, &tmap_u, 0, c * T_TOK, b, &sb->eu_full);
+            tma_load_3d(smem + SM_EU + T_TOK * 128, &tmap_u, 64, c * T_TOK, b, &sb->eu_full);
+#endif
+            eu_last = i;
+        };
+        if (copier && n > 0) load_eu(0);
         for (int i = 0; i < n; ++i) {
             const int r = i % REGIONS;
             int b, c;
@@ -839,35 +845,53 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             const int Tc = min(T_TOK, L - c * T_TOK);
             const size_t row0 = ((size_t)b * L + (size_t)c * T_TOK) * H_F + h;
             unsigned short *yrow = yout + row0;
-            if (!pipe_wait(&sb->eu_full, i & 1, sb, hdr)) break;
-            unsigned short uv[T_TOK];
+            // every exit is taken by the whole warp (the TMEM loads below are
+            // warp-wide instructions)
+            if (!__all_sync(0xffffffffu, pipe_wait(&sb->eu_full, i & 1, sb, hdr))) break;
+            // tokens 2k and 2k+1 packed into uv[k] (low and high half)
+            uint32_t uv[T_TOK / 2];
 #pragma unroll
-            for (int t = 0; t < T_TOK; ++t)
-                uv[t] = *reinterpret_cast<const unsigned short *>(eu + t * 128 + ((((hc >> 3) ^ (uint32_t)(t & 7))) << 4) +
-                                                                  ((hc & 7u) << 1));
+            for (int k = 0; k < T_TOK / 2; ++k) {
+                const uint32_t lo = *reinterpret_cast<const unsigned short *>(
+                    eu + (2 * k) * 128 + ((((hc >> 3) ^ (uint32_t)((2 * k) & 7))) << 4) + ((hc & 7u) << 1));
+                const uint32_t hi = *reinterpret_cast<const unsigned short *>(
+                    eu + (2 * k + 1) * 128 + ((((hc >> 3) ^ (uint32_t)((2 * k + 1) & 7))) << 4) + ((hc & 7u) << 1));
+                uv[k] = lo | (hi << 16);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sb->eu_empty);
-            if (!pipe_wait(&sb->mma2_done[r], (i / REGIONS) & 1, sb, hdr)) break;
+            bool go = true;
+            if (copier && i + 1 < n) {
+                go = pipe_wait(&sb->eu_empty, i & 1, sb, hdr);
+                if (go) load_eu(i + 1);
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!__all_sync(0xffffffffu, go && pipe_wait(&sb->mma2_done[r], (i / REGIONS) & 1, sb, hdr))) break;
             tc_fence_after();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t ya[32];
-                tmem_ld32(lane_base + (uint32_t)r * 128u + (uint32_t)hf * 32u, ya);
+            for (int hf = 0; hf < 4; ++hf) {
+                uint32_t ya[16], yb[16];
+                tmem_ld16(lane_base + (uint32_t)r * 128u + (uint32_t)hf * 16u, ya);
+                tmem_ld16(lane_base + (uint32_t)r * 128u + 64u + (uint32_t)hf * 16u, yb);
                 tmem_wait_ld();
-                if (hf == 1) {
+                if (hf == 3) {
                     // every column of the region has been read: it may be reused
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sb->tmem_empty[r]);
                 }
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int t = hf * 32 + k;
-                    const float v = fmaf(dh, __uint_as_float((uint32_t)uv[t] << 16), __uint_as_float(ya[k]));
+                for (int k = 0; k < 16; ++k) {
+                    const int t = hf * 16 + k;
+                    const uint32_t ub = (t & 1) ? (uv[t >> 1] & 0xFFFF0000u) : (uv[t >> 1] << 16);
+                    const float v = fmaf(dh, __uint_as_float(ub),
+                                         __uint_as_float(ya[k]) + __uint_as_float(yb[k]));
                     if (t < Tc) yrow[(size_t)t * H_F] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
                 }
             }
         }
+        // a copy still in flight (the loop left early) must land before the CTA exits
+        if (copier && eu_last >= 0) drain_wait(&sb->eu_full, eu_last & 1);
     } else if (warp >= W_FOLD && warp < W_FOLD + 4 && W > 1) {
         // ------------------------------------------------------------ carries
         const int m = 32 * (warp - W_FOLD) + lane;
