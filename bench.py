@@ -179,6 +179,78 @@ def algorithmic_bytes(w, u_bytes_per, y_bytes_per):
     return w.B * w.L * w.H * (u_bytes_per + y_bytes_per) + params
 
 
+# Nominal dense TF32 : BF16 tensor rates on GB300 (1.1 : 2.25 PFLOP/s); the
+# fp32 workloads' tensor peak is the measured bf16 peak scaled by it.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def projection_flops(w):
+    """Flops of the two dense projections per launch: B_bar u (complex [P,H]
+    times real u: 4PH per token) and 2 Re(C~ x) (4PH per token; twice that
+    for the bidirectional readout, whose C~ has 2P columns)."""
+    per_token = 4 * w.P * w.H + (8 if w.bidirectional else 4) * w.P * w.H
+    return w.B * w.L * per_token
+
+
+def layer_roofline(w, launch_s, kname, traffic, clocks, num_sms, u_bytes, simt):
+    """The roofline of one layer launch: its time bound is the larger of the
+    algorithmic HBM bytes at the measured copy rate and the projection flops
+    at the measured tensor rate (bf16 projections: bf16; fp32 ones: TF32),
+    and frac = that bound / the measured launch time.  The other term and,
+    for the CUDA-core kernel, the FP32 FMA-pipe fraction are diagnostics."""
+    hbm_gbs, bf16_tf, peak_kind = load_peaks()
+    alg = algorithmic_bytes(w, u_bytes, u_bytes)
+    flops = projection_flops(w)
+    tensor_tf = bf16_tf if w.proj_dtype == "bf16" else bf16_tf * TF32_PER_BF16
+    t_hbm = alg / (hbm_gbs * 1e9)
+    t_tensor = flops / (tensor_tf * 1e12) if tensor_tf else 0.0
+    hbm_bound = t_hbm >= t_tensor
+    src = ("%s (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
+           else "fallback 6.8 TB/s, 1.9 PFLOP/s bf16")
+    r = {
+        "bound": "hbm" if hbm_bound else "tensor",
+        "kernel": kname,
+        "achieved": alg / launch_s / 1e9 if hbm_bound else flops / launch_s / 1e12,
+        "peak": hbm_gbs if hbm_bound else tensor_tf,
+        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "frac": max(t_hbm, t_tensor) / launch_s,
+        "peak_source": src + (": hbm_gbs" if hbm_bound else
+                              ": bf16_tflops" if w.proj_dtype == "bf16" else
+                              ": bf16_tflops x 1.1/2.25 (TF32)"),
+        "definition": "frac = max(algorithmic bytes / HBM peak, projection flops / tensor "
+                      "peak) / launch time",
+        "algorithmic_bytes_per_launch": alg,
+        "projection_flops_per_launch": flops,
+        "hbm_frac": t_hbm / launch_s,
+        "tensor_frac": t_tensor / launch_s,
+        "tensor_peak_tflops": tensor_tf,
+        "launch_us": launch_s * 1e6,
+        "traffic": traffic,
+    }
+    if simt:
+        # diagnostic: the FP32 FMA pipe the CUDA-core kernel runs on (SMs x
+        # 128 lanes x 2 flops per FMA at the sampled SM clock)
+        simt_flops = w.B * w.L * (8 * w.P * w.H + 8 * w.P + 2 * w.H)
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        alu_tf = num_sms * 128 * 2 * mhz * 1e6 / 1e12
+        r.update({"alu_frac": simt_flops / launch_s / 1e12 / alu_tf, "alu_peak_tflops": alu_tf,
+                  "alu_peak_source": "%d SMs (device query) x 128 lanes x 2 flops x %.0f MHz"
+                                     % (num_sms, mhz)})
+    return r
+
+
+def parity_field(got, ref, tol, sample):
+    """rel-L2 and max-abs error of the bench's own output against the oracle."""
+    import numpy as np
+    got = np.asarray(got, np.complex128 if np.iscomplexobj(got) else np.float64)
+    ref = np.asarray(ref, np.complex128 if np.iscomplexobj(ref) else np.float64)
+    err = got - ref
+    rel = float(np.linalg.norm(err) / np.linalg.norm(ref))
+    return {"rel_l2": rel, "max_abs": float(np.max(np.abs(err))),
+            "max_abs_ref": float(np.max(np.abs(ref))), "tol_rel_l2": tol, "pass": rel <= tol,
+            "sample": sample}
+
+
 def graph_event(torch):
     """A timing event that can be recorded inside a CUDA graph capture."""
     try:
@@ -381,10 +453,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return None
 
-    hbm_gbs, _, peak_kind = load_peaks()
     ub = 2 if w.u_dtype == "bf16" else 4
-    alg = algorithmic_bytes(w, ub, ub)
-    achieved = alg / fwd_avg_s / 1e9
     kname = "fwd_tc_kernel" if tc_path else "fwd_simt_kernel"
     src = os.path.join(ROOT, "diagonal_state_space_gb300", "csrc",
                        "s5_forward_tc.cu" if tc_path else "s5_forward_simt.cu")
@@ -395,34 +464,8 @@ def run_ours(args):
         kname = ("bidirectional layer (fwd_tc_kernel + bwd_tc_kernel + split)" if tc_path else
                  "bidirectional layer (2 x %s + split, reverse, add)" % kname)
         traffic = None
-    roofline = {
-        "bound": "hbm",
-        "kernel": kname,
-        "achieved": achieved,
-        "peak": hbm_gbs,
-        "unit": "GB/s",
-        "frac": achieved / hbm_gbs,
-        "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
-                       if peak_kind == "measured" else "fallback 6.8 TB/s",
-        "algorithmic_bytes_per_launch": alg,
-        "launch_us": fwd_avg_s * 1e6,
-        "traffic": traffic,
-    }
-    if not tc_path:
-        # CUDA-core path: the fp32 FMAs take longer than the HBM bytes, so the
-        # roofline is the FP32 pipe (152 SMs x 128 lanes x 2 flops per FMA at
-        # the sampled SM clock); the HBM fraction is kept beside it
-        flops = tokens * (8 * w.P * w.H + 8 * w.P + 2 * w.H)
-        mhz = (clocks or {}).get("sm_mhz") or 2070.0
-        alu_tf = 152 * 128 * 2 * mhz * 1e6 / 1e12
-        roofline.update({
-            "bound": "alu", "achieved": flops / fwd_avg_s / 1e12, "peak": alu_tf,
-            "unit": "TFLOP/s", "frac": flops / fwd_avg_s / 1e12 / alu_tf,
-            "peak_source": "FP32 FMA peak from unit counts: 152 SMs x 128 lanes x 2 flops x "
-                           "%.0f MHz" % mhz,
-            "algorithmic_flops_per_launch": flops,
-            "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_gbs,
-        })
+    num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    roofline = layer_roofline(w, fwd_avg_s, kname, traffic, clocks, num_sms, ub, not tc_path)
     result = {
         "metric": BIDI_METRIC if w.bidirectional else METRIC,
         "value": value,
@@ -470,7 +513,11 @@ def run_ours(args):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, inp)
+        result["cpu_baseline"], oy = cpu_baseline(w, inp)
+        tol = 2e-2 if (w.u_dtype == "bf16" or w.proj_dtype == "bf16") else 1e-5
+        result["parity"] = parity_field(y_sets[0].float().cpu().numpy(), oy, tol,
+                                        "y of a bench step, all %d sequences, against the "
+                                        "float64 oracle" % w.B)
     print(json.dumps(result), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -577,10 +624,12 @@ def run_stream(args):
             dist.destroy_process_group()
         return None
 
-    hbm_gbs, _, peak_kind = load_peaks()
+    hbm_gbs, bf16_tf, peak_kind = load_peaks()
     # per call: lambda_bar, B_bar, C~, D once; the state read and written; u and y
     alg = 8 * w.P + 16 * w.P * w.H + 4 * w.H + 16 * w.B * w.P + 8 * w.B * w.H
     achieved = alg / call_s / 1e9
+    # the projections of one call at the TF32 tensor rate: far below the bytes
+    t_tensor = w.B * 8 * w.P * w.H / (bf16_tf * TF32_PER_BF16 * 1e12) if bf16_tf else 0.0
     result = {
         "metric": STREAM_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -602,6 +651,9 @@ def run_stream(args):
             "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
             "algorithmic_bytes_per_launch": alg, "launch_us": call_s * 1e6, "traffic": None,
+            "tensor_frac": t_tensor / call_s,
+            "definition": "frac = max(algorithmic bytes / HBM peak, projection flops / tensor "
+                          "peak) / call time; the bytes term is the larger",
             "note": "a dependent chain of small launches: bound by launch latency, not bandwidth",
         },
         "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
@@ -610,7 +662,16 @@ def run_stream(args):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, inp)
+        # one pass from the zero state (the timed steps carry the state on)
+        x.zero_()
+        api.s5_discretize(lam, log_dt, bt, lb, bb)
+        for k in range(w.L):
+            api.s5_step(lb, bb, ct, d, x, u_t[k], y=y_t[k])
+        y_bl = y_t.transpose(0, 1).cpu().numpy()
+        result["cpu_baseline"], oy = cpu_baseline(w, inp)
+        result["parity"] = parity_field(y_bl, oy, 1e-5, "y of one pass of %d s5_step calls "
+                                        "from the zero state, all %d sequences, against the "
+                                        "float64 oracle" % (w.L, w.B))
     print(json.dumps(result), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -729,7 +790,16 @@ def run_stack(args):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = stack_cpu_baseline(w, inp)
+        # sequence 0's top-layer output and input gradient depend on that
+        # sequence alone, so the oracle's one-sequence run checks them
+        u_top = st.forward(u0)[0].float().cpu().numpy()
+        du0 = st.backward(G)["du0"][0].float().cpu().numpy()
+        torch.cuda.synchronize()
+        result["cpu_baseline"], (ou, og) = stack_cpu_baseline(w, inp)
+        result["parity"] = {
+            "u_out": parity_field(u_top, ou[0], 2e-2, "sequence 0, top-layer output"),
+            "du0": parity_field(du0, og["du0"][0], 2e-2, "sequence 0, input gradient"),
+        }
     print(json.dumps(result), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -747,11 +817,12 @@ def stack_cpu_baseline(w, inp):
     """The float64 oracle stack (forward + backward), single-threaded, on one
     sequence of the workload."""
     t0 = time.perf_counter()
-    oracle_stack_run(inp, [0])
+    out = oracle_stack_run(inp, [0])
     dt = time.perf_counter() - t0
-    return {"value": w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "1 sequence x %d tokens (of %d), %d layers forward + backward, %.1f s"
-                      % (w.L, w.B, w.layers, dt), "host_cores_available": os.cpu_count()}
+    rec = {"value": w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": "1 sequence x %d tokens (of %d), %d layers forward + backward, %.1f s"
+                     % (w.L, w.B, w.layers, dt), "host_cores_available": os.cpu_count()}
+    return rec, out
 
 
 def run_reference_stack(args):
@@ -800,15 +871,18 @@ def oracle_run(w, inp, seqs):
 
 
 def cpu_baseline(w, inp):
-    """The float64 oracle, as it stands, single-threaded on one host core."""
+    """The float64 oracle, as it stands, single-threaded on one host core.
+    Returns the baseline record and the oracle's y (every sequence), against
+    which the bench's own output is then compared."""
     seqs = list(range(w.B))
     t0 = time.perf_counter()
-    oracle_run(w, inp, seqs)
+    out = oracle_run(w, inp, seqs)
     dt = time.perf_counter() - t0
-    return {"value": len(seqs) * w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": "the whole workload (%d sequences x %d tokens), one pass, %.1f s"
-                      % (len(seqs), w.L, dt),
-            "host_cores_available": os.cpu_count()}
+    rec = {"value": len(seqs) * w.L / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": "the whole workload (%d sequences x %d tokens), one pass, %.1f s"
+                     % (len(seqs), w.L, dt),
+           "host_cores_available": os.cpu_count()}
+    return rec, (out[0] if isinstance(out, tuple) else out)
 
 
 def run_reference(args):
@@ -846,8 +920,39 @@ def run_reference(args):
     return res
 
 
+def launch_replicas(args, argv):
+    """``--gpus N``: inside a torchrun rank, WORLD_SIZE must equal N; run
+    directly with N > 1, start N ranks of this script (one per GPU, replicas)
+    under torch.distributed.run on 127.0.0.1 and return their exit status.
+    Returns None when this process should run the bench itself."""
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is not None:
+        if int(world_env) != args.gpus:
+            sys.exit("bench.py: --gpus %d but WORLD_SIZE=%s; launch exactly --gpus ranks "
+                     "(torchrun --nproc-per-node N bench.py --gpus N)" % (args.gpus, world_env))
+        return None
+    if args.gpus < 1:
+        sys.exit("bench.py: --gpus must be at least 1")
+    if args.gpus == 1:
+        return None
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           "--nproc-per-node", str(args.gpus), "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     args = parse()
+    rc = launch_replicas(args, sys.argv[1:])
+    if rc is not None:
+        sys.exit(rc)
+    world, rank, _ = dist_env()
+    if world > 1:
+        print("bench: rank %d of %d" % (rank, world), file=sys.stderr, flush=True)
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "stack6":

@@ -178,6 +178,10 @@ s5_status run_tc_backward_add(const float2 *lambda_bar, const float2 *b_bar, con
 
 }  // namespace
 
+namespace s5 {
+s5_status cuda_failure(cudaError_t e) { return cuda_fail(e); }
+}  // namespace s5
+
 extern "C" {
 
 const char *s5_status_string(s5_status s) {

@@ -10,6 +10,10 @@
 
 namespace s5 {
 
+// Records a CUDA error as the text s5_last_cuda_error() returns and gives
+// S5_ERR_CUDA (defined with the entry points in s5_api.cu).
+s5_status cuda_failure(cudaError_t e);
+
 // ---------------------------------------------------------------------------
 // Workspace.  The chunked scan publishes, per tile of T tokens of one
 // sequence, the tile's aggregate map (A, E) = (product of a_k, end state from a

@@ -202,18 +202,22 @@ size_t s5_workspace_size(int B, int L, int H, int P);
  * memory (a plugin in a host application that owns all device memory, a
  * latency-critical loop that must not enter the allocator, an embedded
  * deployment with a fixed memory budget).  The paper has no counterpart.
- * Arguments, layouts and results are those of s5_forward; the caller still
- * passes every input and output.  The carry scratch is a fixed device array
- * of S5_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
- * it until the process exits.
+ * Arguments, layouts, dtypes, results and errors are those of s5_forward,
+ * including its choice of kernel: bf16 u, y and projections at H = P = 128
+ * run the tensor-core kernel, everything else the CUDA-core kernel.  The
+ * caller still passes every input and output.  The workspace is a fixed
+ * device array of S5_NOALLOC_SCRATCH_BYTES inside the library (zeroed when
+ * the library loads), held on every GPU that loads it until the process
+ * exits.
  *  - Sizes whose s5_workspace_size(B,L,H,P) exceeds S5_NOALLOC_SCRATCH_BYTES
  *    are rejected with S5_ERR_INVALID_ARGUMENT before anything is queued.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.
- *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
- *    library routine.  It clears the scratch's header and flags on `stream`
- *    (cudaMemsetAsync) and launches the CUDA-core forward kernel.
+ *  - The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ *    library routine) and clears nothing: like any workspace, the array needs
+ *    no clearing between calls.  It queues the same kernels as s5_forward.
+ *  - A failed CUDA call returns S5_ERR_CUDA, its text in s5_last_cuda_error().
  *  - Every call shares the one array: calls that overlap on the GPU (other
  *    streams, other host threads) race and give wrong results.  Serialize them.
  *  - Device-side conditions (a carry wait that gave up) are not reported.

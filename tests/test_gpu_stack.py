@@ -10,7 +10,7 @@ import oracle
 from diagonal_state_space_gb300 import stack as s5stack
 from diagonal_state_space_gb300.workloads import make_stack_inputs
 
-from _parity import dev, rel_l2
+from _parity import dev, check
 
 pytestmark = pytest.mark.gpu
 BF16_TOL = 2e-2
@@ -40,7 +40,7 @@ def test_layernorm_matches_oracle(N, H):
     z16 = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
     z = s5stack.layernorm(dev(x), z_bf16=z16)
     oz = oracle.layernorm(x)
-    assert rel_l2(_host(z), oz) <= 1e-5
+    check(_host(z), oz, 1e-5, "_host(z)")
     assert torch.equal(z16, z.to(torch.bfloat16))
 
 
@@ -53,10 +53,9 @@ def test_stack_forward_backward_matches_oracle(B, L, H, P, nl):
     g = st.backward(dev(inp["G"]))
     torch.cuda.synchronize()
     ou, og = oracle.stack(_oracle_params(inp["params"]), inp["u0"], inp["G"])
-    assert rel_l2(_host(u), ou) <= BF16_TOL
+    check(_host(u), ou, BF16_TOL, "_host(u)")
     for k in GRADS:
-        e = rel_l2(_host(g[k]), og[k])
-        assert e <= BF16_TOL, (k, e)
+        check(_host(g[k]), og[k], BF16_TOL, k)
 
 
 def test_stack_full_size_sampled_sequence():
@@ -74,13 +73,12 @@ def test_stack_full_size_sampled_sequence():
     g = st.backward(dev(G))
     torch.cuda.synchronize()
     ou, og = oracle.stack(_oracle_params(inp["params"]), inp["u0"][:1], G[:1])
-    assert rel_l2(u0_host, ou[0]) <= BF16_TOL
+    check(u0_host, ou[0], BF16_TOL, "u0_host")
     du0 = _host(g["du0"])
-    assert rel_l2(du0[:1], og["du0"]) <= BF16_TOL
+    check(du0[:1], og["du0"], BF16_TOL, "du0[:1]")
     assert not np.any(du0[1:])
     for k in GRADS[1:]:
-        e = rel_l2(_host(g[k]), og[k])
-        assert e <= BF16_TOL, (k, e)
+        check(_host(g[k]), og[k], BF16_TOL, k)
 
 
 def test_stack_rejects_misaligned_and_oversize():

@@ -8,7 +8,7 @@ import torch
 from diagonal_state_space_gb300 import api
 from diagonal_state_space_gb300.workloads import make_layer_inputs
 
-from _parity import dev, host, layer_to_device, oracle_forward, rel_l2
+from _parity import check, dev, host, layer_to_device, oracle_forward
 
 pytestmark = pytest.mark.gpu
 BF16_TOL = 2e-2
@@ -41,16 +41,16 @@ def _run(B, L, seed, zero_d=False, x0=None):
 @pytest.mark.parametrize("zero_d", [False, True])
 def test_tc_forward_matches_oracle(B, L, zero_d):
     y, oy, xl, oxl = _run(B, L, seed=31 * B + L, zero_d=zero_d)
-    assert rel_l2(y, oy) <= BF16_TOL
-    assert rel_l2(xl, oxl) <= BF16_TOL
+    check(y, oy, BF16_TOL, "y")
+    check(xl, oxl, BF16_TOL, "xl")
 
 
 def test_tc_forward_with_initial_state():
     rng = np.random.default_rng(5)
     x0 = (rng.standard_normal((4, 128)) + 1j * rng.standard_normal((4, 128))).astype(np.complex64)
     y, oy, xl, oxl = _run(4, 777, seed=12, zero_d=True, x0=x0)
-    assert rel_l2(y, oy) <= BF16_TOL
-    assert rel_l2(xl, oxl) <= BF16_TOL
+    check(y, oy, BF16_TOL, "y")
+    check(xl, oxl, BF16_TOL, "xl")
 
 
 def test_tc_repeat_calls_share_a_workspace():
@@ -63,8 +63,8 @@ def test_tc_repeat_calls_share_a_workspace():
     assert api.s5_sync_status(ws) == 0
     oy, _ = oracle_forward(inp)
     for o in outs:
-        assert rel_l2(o, oy) <= BF16_TOL
-    assert rel_l2(outs[1], outs[2]) <= 1e-3
+        check(o, oy, BF16_TOL, "o")
+    check(outs[1], outs[2], 1e-3, "outs[1]")
 
 
 def test_tc_back_to_back_layers_match_synchronised_calls():
@@ -98,10 +98,10 @@ def test_tc_back_to_back_layers_match_synchronised_calls():
     for _ in range(2):
         c1, c2 = two_layers(sync=False)
         s1, s2 = two_layers(sync=True)
-        assert rel_l2(c1, s1) <= 1e-3
-        assert rel_l2(c2, s2) <= 1e-3
+        check(c1, s1, 1e-3, "c1")
+        check(c2, s2, 1e-3, "c2")
     oy1, _ = oracle_forward(inp1)
-    assert rel_l2(c1, oy1) <= BF16_TOL
+    check(c1, oy1, BF16_TOL, "c1")
 
 
 def test_tc_carry_wait_timeout_is_reported_and_recoverable():
@@ -118,4 +118,4 @@ def test_tc_carry_wait_timeout_is_reported_and_recoverable():
     words[5] = 0
     y = api.s5_forward(lb, bb, t["c_tilde"], t["d"], t["u"], proj_dtype="bf16", workspace=ws)
     assert api.s5_sync_status(ws) == 0
-    assert rel_l2(host(y), oracle_forward(inp)[0]) <= BF16_TOL
+    check(host(y), oracle_forward(inp)[0], BF16_TOL, "host(y)")

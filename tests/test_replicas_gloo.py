@@ -60,3 +60,34 @@ def test_single_process_needs_no_process_group():
 
     assert bench.max_over_ranks(12.5, None) == 12.5
     assert bench.job_throughput(131072, 1, 56.0) == 131072 / 0.056
+
+
+def test_gpus_flag_starts_that_many_ranks():
+    """bench.py --gpus 2, run directly, starts two ranks under
+    torch.distributed.run; rank 0 alone prints the line, with n_gpus 2 (the
+    oracle arm, which needs no GPU)."""
+    import json
+    import subprocess
+
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl",
+                          "reference", "--workload", "small", "--steps", "1", "--warmup", "1"],
+                         capture_output=True, text=True, env=env, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(l) for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+    assert "bench: rank 0 of 2" in res.stderr and "bench: rank 1 of 2" in res.stderr
+
+
+def test_gpus_flag_must_match_the_launched_ranks():
+    import subprocess
+
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "4", "--impl",
+                          "reference", "--workload", "small"],
+                         capture_output=True, text=True, env=env, timeout=300)
+    assert res.returncode != 0
+    assert "--gpus 4 but WORLD_SIZE=2" in res.stderr
