@@ -1,47 +1,82 @@
-// s5_discretize.cu -- zero-order-hold discretisation of the diagonal modes.
-//
-// "SIMPLIFIED STATE SPACE LAYERS FOR SEQUENCE MODELING", section 3.2 eq. 6, and
-// the abhik.ai review "S5: Simplified State Space Layers for Sequence Modeling",
-// "Paper equations beside executable Python" row 2:
-//   lambda_bar = exp(lambda*Delta),  B_bar = (lambda_bar - 1)/lambda * B_tilde,
-// where (lambda_bar - 1)/lambda = Delta*phi1(lambda*Delta), phi1(z) = (e^z-1)/z,
-// has a removable singularity at z = 0 (limit Delta).
-//
-// The per-mode factors are computed in float64 (only P values per call) with
-// a complex expm1, e^z - 1 = expm1(x)cos(y) - 2 sin^2(y/2) + i e^x sin(y), so
-// that small |z| loses no digits; below |z| = 1e-4 a Taylor series of phi1 is
-// used instead, as the review's reference does.
+// The per-mode factors are computed in float-float arithmetic (s5_ff.cuh:
+// about 48 significant bits from FP32 instructions) and rounded once to
+// float, so they agree with a float64 evaluation to within one rounding.
+// The phase Im(lambda)*Delta reaches tens of radians, so it needs more than
+// float precision before its sine and cosine are taken; GB300's float64 pipe
+// is too slow for the latency-bound chain (exp, then sin/cos, then a divide)
+// that each mode is.  A complex expm1 keeps small |z| exact:
+//   e^z - 1 = (e^x cos y - 1) + i e^x sin y,
+//   e^x cos y - 1 = expm1(x) - vers(y) - expm1(x) vers(y),  vers = 1 - cos,
+// with expm1 and vers from their own series (no cancellation near 0); the
+// quotient by lambda then tends to Delta as z -> 0 without a separate branch.
 #include "s5_internal.cuh"
+#include "s5_ff.cuh"
 
 namespace s5 {
 
-struct dcplx { double re, im; };
+namespace {
 
-__device__ inline dcplx dmul(dcplx a, dcplx b) {
-    return {a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
-}
-__device__ inline dcplx ddiv(dcplx a, dcplx b) {
-    double den = b.re * b.re + b.im * b.im;
-    return {(a.re * b.re + a.im * b.im) / den, (a.im * b.re - a.re * b.im) / den};
+// Options of s5_discretize_ex, as float-float values.
+struct DiscOpts {
+    int method;          // 0 zero-order hold, 1 bilinear
+    int clip_on;         // clip_eigs: Re(lambda) <- min(Re(lambda), clip)
+    ff::F2 clip, scale;  // clip threshold; Delta multiplier (1 when not rescaling)
+};
+
+// lambda_bar (rounded) and the gain g = (lambda_bar - 1)/lambda (ZOH) or
+// Delta/(1 - Delta lambda/2) (bilinear), g in float-float.
+__device__ __forceinline__ void mode_factors(float2 l, float log_dt, const DiscOpts &o, float2 &lbar,
+                                             ff::F2 &g_re, ff::F2 &g_im) {
+    using namespace ff;
+    F2 lr = make(l.x);
+    const float li = l.y;
+    // Re(lambda) > clip, compared exactly in float-float
+    if (o.clip_on && (l.x > o.clip.hi || (l.x == o.clip.hi && o.clip.lo < 0.f))) lr = o.clip;
+    F2 dt, unused;
+    exp_expm1(make(log_dt), dt, unused);
+    dt = mul(dt, o.scale);
+    const F2 zr = mul(lr, dt), zi = mul(dt, li);
+    if (o.method == 1) {
+        // lambda_bar = (1 + z/2) / (1 - z/2), g = Delta / (1 - z/2)
+        const F2 hr = mul(zr, 0.5f), hi = mul(zi, 0.5f);
+        const F2 nr = add(make(1.f), hr), dr = sub(make(1.f), hr);
+        // 1/(dr - i hi) = (dr + i hi) / (dr^2 + hi^2)
+        const F2 inv = recip(add(mul(dr, dr), mul(hi, hi)));
+        lbar = make_float2(to_float(mul(sub(mul(nr, dr), mul(hi, hi)), inv)),
+                           to_float(mul(add(mul(hi, dr), mul(nr, hi)), inv)));
+        g_re = mul(mul(dt, dr), inv);
+        g_im = mul(mul(dt, hi), inv);
+        return;
+    }
+    F2 ez, em1, sn, cs, vs;
+    exp_expm1(zr, ez, em1);
+    sincos_vers(zi, sn, cs, vs);
+    lbar = make_float2(to_float(mul(ez, cs)), to_float(mul(ez, sn)));
+    if (lr.hi == 0.f && li == 0.f) {
+        // the removable singularity: (e^z - 1)/lambda -> Delta
+        g_re = dt;
+        g_im = make(0.f);
+        return;
+    }
+    const F2 A = sub(sub(em1, vs), mul(em1, vs));   // Re(e^z - 1)
+    const F2 Bm = mul(ez, sn);                       // Im(e^z - 1)
+    // (A + iB) / (lr + i li) = ((A lr + B li) + i (B lr - A li)) / |lambda|^2
+    const F2 inv = recip(add(mul(lr, lr), two_prod(li, li)));
+    g_re = mul(add(mul(A, lr), mul(Bm, li)), inv);
+    g_im = mul(sub(mul(Bm, lr), mul(A, li)), inv);
 }
 
-// One block per mode (float64 throughput per SM is small, so the work is
-// spread over P SMs).  The float64 functions of the mode's factors run side by
-// side on the first lane of four different warps (lanes of one warp taking
-// different branches would run them one after another):
-//   every thread  dt = exp(log_dt)
-//   warp 0  sin(Im z), cos(Im z)      warp 1  exp(Re z)
-//   warp 2  expm1(Re z)               warp 3  sin(Im z / 2)
-//   warp 4  1 / lambda
-// then lambda_bar = e^Re z (cos, sin) and, for |z| >= 1e-4,
-// (e^z - 1)/lambda = (expm1(Re z) cos(Im z) - 2 sin^2(Im z/2) + i e^Re z sin(Im z)) * (1/lambda);
-// below |z| = 1e-4, Delta * phi1(z) from its Taylor series.  Every thread of
-// the block then scales a slice of the B_tilde row.  Blocks have >= 160 threads.
+}  // namespace
+
+// One block per mode; every thread computes the mode's factors (the same
+// values in every lane: no barrier, no shared memory) and then scales its
+// slice of the B_tilde row:  B_bar = g * B_tilde, formed in float-float and
+// rounded once.
 //
-// Options (all in float64, applied before the factors above):
-//   clip_re != 0   clip_eigs: Re(lambda) <- min(Re(lambda), clip_re)
+// Options (applied before the factors above):
+//   clip_on        clip_eigs: Re(lambda) <- min(Re(lambda), clip_re)
 //                  (wikillm "Paper vs code": the official value is -1e-4);
-//   dt_scale       sampling-rate rescaling, Delta <- Delta * dt_scale with
+//   scale          sampling-rate rescaling, Delta <- Delta * dt_scale with
 //                  dt_scale = old rate / new rate (review "Sampling intervals
 //                  carry physical meaning"; summary section 6.2);
 //   method 1       bilinear transform instead of the zero-order hold (review
@@ -51,85 +86,33 @@ __device__ inline dcplx ddiv(dcplx a, dcplx b) {
 //                  gain = Delta / (1 - Delta lambda/2).
 __global__ void discretize_kernel(const float2 *__restrict__ lambda, const float *__restrict__ log_dt,
                                   const float2 *__restrict__ b_tilde, int P, int H,
-                                  float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar, int method,
-                                  double clip_re, double dt_scale) {
+                                  float2 *__restrict__ lambda_bar, float2 *__restrict__ b_bar,
+                                  const DiscOpts opts) {
     const int p = blockIdx.x;
     // the kernel that consumes Lambda_bar and B_bar may be scheduled now; it
     // waits for this one to complete before reading them
     griddep_launch_dependents();
-    __shared__ double s_f[7];      // sin Im z, cos Im z, exp Re z, expm1 Re z, sin(Im z / 2), 1/lambda
-    __shared__ double s_gain[2];
-    // Only the first lane of each of the first five warps needs Delta and z:
-    // float64 work on the other lanes would still occupy the SM's few float64
-    // units, so they skip it.
-    const bool leader = (threadIdx.x & 31) == 0 && threadIdx.x < 160;
-    // this thread's first B_tilde element, fetched now so that its latency
-    // overlaps the float64 work below
+    // Launched programmatically, this kernel may start while the kernel
+    // before it still runs: it reads only its inputs (lambda, log_dt,
+    // B_tilde, which the kernels of this library never write) before the
+    // wait below, and writes Lambda_bar and B_bar, which that kernel may
+    // still be reading, only after it.
     const float2 *src = b_tilde + (size_t)p * H;
+    // this thread's first B_tilde element, fetched now so that its latency
+    // overlaps the arithmetic below
     const float2 bt0 = (int)threadIdx.x < H ? src[threadIdx.x] : make_float2(0.f, 0.f);
-    dcplx lam = {0.0, 0.0}, z = {0.0, 0.0};
-    double dt = 0.0;
-    if (leader) {
-        const float2 l = lambda[p];
-        lam = {(double)l.x, (double)l.y};
-        if (clip_re != 0.0 && lam.re > clip_re) lam.re = clip_re;
-        dt = exp((double)log_dt[p]) * dt_scale;
-        z = {lam.re * dt, lam.im * dt};
-    }
-    if (method == 1) {
-        if (threadIdx.x == 0) {
-            const dcplx den = {1.0 - 0.5 * z.re, -0.5 * z.im};
-            const dcplx lb = ddiv(dcplx{1.0 + 0.5 * z.re, 0.5 * z.im}, den);
-            const dcplx gain = ddiv(dcplx{dt, 0.0}, den);
-            lambda_bar[p] = make_float2((float)lb.re, (float)lb.im);
-            s_gain[0] = gain.re;
-            s_gain[1] = gain.im;
-        }
-    } else if (leader) {
-        const int w = threadIdx.x >> 5;
-        if (w == 0) sincos(z.im, &s_f[0], &s_f[1]);
-        else if (w == 1) s_f[2] = exp(z.re);
-        else if (w == 2) s_f[3] = expm1(z.re);
-        else if (w == 3) s_f[4] = sin(0.5 * z.im);
-        else if (w == 4) {
-            // 1/lambda, off the path of the functions above
-            const double den = lam.re * lam.re + lam.im * lam.im;
-            s_f[5] = lam.re / den;
-            s_f[6] = -lam.im / den;
-        }
-    }
-    __syncthreads();
-    if (method != 1 && threadIdx.x == 0) {
-        const double s = s_f[0], c = s_f[1], mag = s_f[2], em1r = s_f[3], sh = s_f[4];
-        dcplx gain;
-        const double zabs = sqrt(z.re * z.re + z.im * z.im);
-        if (zabs < 1e-4) {
-            // dt * (1 + z/2 + z^2/6 + z^3/24 + z^4/120); the next term is below 1e-22.
-            dcplx term = {1.0, 0.0}, phi = {1.0, 0.0};
-            for (int n = 1; n <= 4; ++n) {
-                term = dmul(term, z);
-                const double f = 1.0 / (double)(n + 1);
-                term.re *= f;
-                term.im *= f;
-                phi.re += term.re;
-                phi.im += term.im;
-            }
-            gain = {dt * phi.re, dt * phi.im};
-        } else {
-            const dcplx em1 = {em1r * c - 2.0 * sh * sh, mag * s};
-            gain = dmul(em1, dcplx{s_f[5], s_f[6]});
-        }
-        lambda_bar[p] = make_float2((float)(mag * c), (float)(mag * s));
-        s_gain[0] = gain.re;
-        s_gain[1] = gain.im;
-    }
-    __syncthreads();
-    const dcplx g = {s_gain[0], s_gain[1]};
+    float2 lb;
+    ff::F2 g_re, g_im;
+    mode_factors(lambda[p], log_dt[p], opts, lb, g_re, g_im);
+    griddep_wait();
+    if (threadIdx.x == 0) lambda_bar[p] = lb;
     float2 *dst = b_bar + (size_t)p * H;
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
         const float2 bt = h == (int)threadIdx.x ? bt0 : src[h];
-        const dcplx v = dmul(g, dcplx{(double)bt.x, (double)bt.y});
-        dst[h] = make_float2((float)v.re, (float)v.im);
+        using namespace ff;
+        const F2 re = sub(mul(g_re, bt.x), mul(g_im, bt.y));
+        const F2 im = add(mul(g_re, bt.y), mul(g_im, bt.x));
+        dst[h] = make_float2(to_float(re), to_float(im));
     }
 }
 
@@ -158,10 +141,22 @@ __global__ void mode_consts_kernel(const float2 *__restrict__ lambda, const floa
 cudaError_t launch_discretize(const float2 *lambda, const float *log_dt, const float2 *b_tilde,
                               int P, int H, float2 *lambda_bar, float2 *b_bar, cudaStream_t st, int method,
                               double clip_re, double dt_scale) {
-    const int threads = H >= 256 ? 256 : 160;   // at least five warps (see discretize_kernel)
-    discretize_kernel<<<P, threads, 0, st>>>(lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar, method, clip_re,
-                                             dt_scale);
-    return cudaGetLastError();
+    DiscOpts o;
+    o.method = method;
+    o.clip_on = clip_re != 0.0;
+    o.clip.hi = (float)clip_re;
+    o.clip.lo = (float)(clip_re - (double)o.clip.hi);
+    o.scale.hi = (float)dt_scale;
+    o.scale.lo = (float)(dt_scale - (double)o.scale.hi);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P);
+    cfg.blockDim = dim3(H >= 256 ? 256 : (unsigned)((H + 31) / 32 * 32));
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    set_programmatic(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, discretize_kernel, lambda, log_dt, b_tilde, P, H, lambda_bar, b_bar, o);
 }
 
 cudaError_t launch_mode_consts(const float2 *lambda, const float *log_dt, int P, ModeConst *out,

@@ -73,6 +73,7 @@ constexpr int REGIONS = 4;              // TMEM regions of 128 columns
 constexpr int THREADS = 512;
 constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;
 constexpr int W_MAX = 64;               // lanes per sequence at most
+constexpr int TC_FREE_SMS = 8;          // SMs left to the next kernel (see tc_grid)
 constexpr int RB = 18;                  // aggregate records loaded per round
 constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps
 
@@ -547,6 +548,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
     unsigned char *smem = smem_raw + pad;
     Bars *sb = reinterpret_cast<Bars *>(smem + SM_BAR);
+    // A kernel launched programmatically after this one (the next layer's
+    // discretisation, say) may be scheduled at once: its blocks take SMs as
+    // this kernel's CTAs exit, and it waits for this grid before touching
+    // anything this grid reads or writes.
+    griddep_launch_dependents();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WsHeader *hdr = args.ws.hdr;
@@ -983,8 +989,13 @@ bool tc_supported(int H, int P, bool u_bf16, bool y_bf16, bool proj_bf16) {
 // Lanes per sequence and grid: W lanes plus one scanner per sequence, B*(W+1)
 // CTAs (2 <= W <= nchunks, W <= W_MAX), when at least three CTAs per sequence
 // fit on the SMs; else W = 1, min(B, SMs) CTAs, each taking whole sequences.
+// TC_FREE_SMS SMs stay out of the grid: the kernel launched after this one
+// (programmatically) becomes resident there while this grid runs, so that
+// its start -- instructions fetched into cold caches, its first loads --
+// overlaps this kernel instead of following it.
 void tc_grid(int B, int nchunks, int num_sms, int *W, int *G) {
-    int w = B <= num_sms ? num_sms / B - 1 : 0;
+    const int usable = num_sms > 2 * TC_FREE_SMS ? num_sms - TC_FREE_SMS : num_sms;
+    int w = B <= usable ? usable / B - 1 : 0;
     if (w > nchunks) w = nchunks;
     if (w > W_MAX) w = W_MAX;
     if (w >= 2) {

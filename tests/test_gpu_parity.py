@@ -50,6 +50,29 @@ def test_discretize_matches_oracle(P, H):
     np.testing.assert_allclose(host(bb), obb, rtol=3e-7, atol=1e-12)
 
 
+def test_discretize_large_phases_and_options():
+    """Modes whose phase Im(lambda)*Delta runs to ~120 rad, strongly damped
+    modes, and every option path, against the float64 oracle at the same
+    bars (lambda_bar 2e-7 relative per element, B_bar 3e-7)."""
+    rng = np.random.default_rng(21)
+    n = np.arange(128)
+    lam = np.concatenate([-0.5 + 1j * np.pi * n,
+                          rng.normal(0, 3, 128) - 0.1 + 1j * rng.normal(0, 400, 128),
+                          -rng.uniform(0.5, 40, 32) + 1j * rng.uniform(-5, 5, 32)]).astype(np.complex64)
+    P = lam.shape[0]
+    log_dt = rng.uniform(np.log(1e-3), np.log(3e-1), P).astype(np.float32)
+    H = 40
+    bt = (rng.standard_normal((P, H)) + 1j * rng.standard_normal((P, H))).astype(np.complex64)
+    for method, clip_re, dt_scale in [("zoh", 0.0, 1.0), ("bilinear", 0.0, 1.0), ("zoh", -1e-4, 0.37),
+                                      ("bilinear", -1e-4, 2.5)]:
+        lb, bb = api.s5_discretize_ex(dev(lam), dev(log_dt), dev(bt), method, clip_re, dt_scale)
+        # the C ABI takes clip_re and dt_scale as float: the oracle gets the same values
+        olb, obb = oracle.discretize_ex(lam, log_dt, bt, method, float(np.float32(clip_re)),
+                                        float(np.float32(dt_scale)))
+        np.testing.assert_allclose(host(lb), olb, rtol=2e-7, atol=1e-30)
+        np.testing.assert_allclose(host(bb), obb, rtol=3e-7, atol=1e-30)
+
+
 def test_discretize_zero_pole_and_tiny_interval():
     lam = np.array([0.0, -0.5 + 1e-3j, -0.5 + 100j, -1e-6], np.complex64)
     log_dt = np.log(np.array([0.37, 1e-6, 0.1, 1e-3])).astype(np.float32)

@@ -137,3 +137,67 @@ def test_traffic_is_reported_only_for_the_captured_source_and_workload(tmp_path,
     src.write_text("// kernel source, edited\n")                     # changed since the capture
     assert bench.traffic_for("k", str(src), "pathx_bf16") is None
 
+
+
+# --------------------------------------------------------------------------
+# The float-float constants of the discretisation kernel (csrc/s5_ff.cuh):
+# 1/n! pairs and the three-part splits of ln 2 and pi/2, checked against the
+# exact rationals (pi from Machin's formula, ln 2 from sum 1/(k 2^k)).
+# --------------------------------------------------------------------------
+def _ff_header():
+    path = os.path.join(ROOT, "diagonal_state_space_gb300", "csrc", "s5_ff.cuh")
+    return open(path).read()
+
+
+def _hexf(tok):
+    tok = tok.rstrip("f")
+    return float.fromhex(tok) if "x" in tok else float(tok)
+
+
+def test_ff_inverse_factorials_are_exact_to_float_float():
+    import math
+    import re
+    from fractions import Fraction
+
+    src = _ff_header()
+    pairs = re.findall(r"case (\d+): return \{([-0-9a-fx.p+]+)f?, ([-0-9a-fx.p+]+)f?\};", src)
+    assert len(pairs) == 17
+    for n, hi, lo in pairs:
+        exact = Fraction(1, math.factorial(int(n)))
+        hi, lo = Fraction(_hexf(hi)), Fraction(_hexf(lo))
+        # hi is the nearest float; hi + lo within 2^-48 of 1/n! (relative)
+        assert abs(hi - exact) <= exact * Fraction(1, 2 ** 24)
+        assert abs(hi + lo - exact) <= exact * Fraction(1, 2 ** 48)
+
+
+def test_ff_cody_waite_splits():
+    import re
+    from decimal import Decimal, getcontext
+    from fractions import Fraction
+
+    getcontext().prec = 60
+
+    def atan_inv(n):
+        x, s, k = Decimal(1) / n, Decimal(0), 0
+        t = x
+        while abs(t) > Decimal(10) ** -58:
+            s += (t / (2 * k + 1)) * (1 if k % 2 == 0 else -1)
+            t *= x * x
+            k += 1
+        return s
+
+    pi = 16 * atan_inv(5) - 4 * atan_inv(239)
+    ln2 = sum(Decimal(1) / (k * Decimal(2) ** k) for k in range(1, 200))
+    src = _ff_header()
+
+    def consts(name):
+        m = re.search(name + r"_1 = ([-0-9a-fx.p+]+)f, " + name + r"_2 = ([-0-9a-fx.p+]+)f, "
+                      + name + r"_3 = ([-0-9a-fx.p+]+)f;", src)
+        return [Fraction(_hexf(t)) for t in m.groups()]
+
+    for name, exact in (("LN2", Fraction(ln2)), ("PIO2", Fraction(pi / 2))):
+        c1, c2, c3 = consts(name)
+        assert abs(c1 + c2 + c3 - exact) <= exact * Fraction(1, 2 ** 64)
+        # the first part has at most 12 significant bits
+        m, e = c1.numerator, c1.denominator
+        assert e & (e - 1) == 0 and m < 2 ** 12
