@@ -75,7 +75,6 @@ constexpr int W_TMEM = 2, W_SCAN = 4, W_EPI = 8, W_FOLD = 12;
 constexpr int W_MAX = 64;               // lanes per sequence at most
 constexpr int TC_FREE_SMS = 8;          // SMs left to the next kernel (see tc_grid)
 constexpr int RB = 18;                  // aggregate records loaded per round
-constexpr uint32_t BAR_SCAN = 1;        // named barrier of the four scan warps
 
 constexpr uint32_t BS_BYTES = 2 * 2 * P_M * 128;       // [2 kb][2P rows][128 B]
 constexpr uint32_t CP_BYTES = 4 * H_F * 128;           // [4 kb][H rows][128 B]
@@ -100,7 +99,7 @@ constexpr unsigned long long DRAIN_WAIT_NS = 200000000ull;   // 0.2 s per teardo
 struct Bars {
     uint64_t full_u[STAGES], empty_u[STAGES];
     uint64_t eu_full, eu_empty;     // the epilogue's u buffer
-    uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], p2read[REGIONS], mma2_done[REGIONS];
+    uint64_t tmem_full[REGIONS], tmem_empty[REGIONS], mma2_done[REGIONS];
     uint64_t xready, xfree;         // X written by the four scan warps / read by GEMM2
     uint64_t weights, drain;
     uint64_t carry_full[2], carry_empty[2];
@@ -124,7 +123,7 @@ __device__ __forceinline__ void set_abort(Bars *sb, WsHeader *hdr) {
 // completes, so it takes no issue slots from the warps sharing its SM
 // sub-partition.
 constexpr uint32_t SLEEP_HINT_NS = 1000000;   // re-check abort/limits every 1 ms
-__device__ __noinline__ bool pipe_wait_slow(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
+__device__ __forceinline__ bool pipe_wait_slow(uint64_t *bar, uint32_t parity, Bars *sb, WsHeader *hdr) {
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS)) return true;
@@ -144,21 +143,6 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
     while (!mbar_try_wait_sleep(bar, parity, SLEEP_HINT_NS))
         if (global_ns() - t0 > DRAIN_WAIT_NS) return false;
     return true;
-}
-
-// Barrier of `threads` threads that also returns the AND of `v` over them, so
-// that the warps taking part leave a loop together.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(threads)
-        : "memory");
-    return r != 0;
 }
 
 // Byte offset of bf16 element (row, col) in a K-major 128-byte-swizzle region
@@ -374,19 +358,12 @@ __device__ __noinline__ float2 pass1_short(uint32_t col0, int Tc, float2 lb) {
     return e;
 }
 
-// Signals that this warp has finished reading the tile's Bu columns.
-__device__ __forceinline__ void bu_read_done(uint64_t *bar) {
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 // Full tile, pass 2: the four chains start from the carry S and
 // S_{q+1} = L S_q + e_q; every state goes as bf16 (Re, Im) into row t of X
 // (row t at xb[t & 7] + (t >> 3) * 1024).  `done` is arrived once the last
 // Bu column is in registers.  Returns the state after token 63.
 __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)[8], const ScanConsts &k,
-                                             float2 S, const float2 (&e)[3], uint64_t *done) {
+                                             float2 S, const float2 (&e)[3]) {
     float2 s0 = S;
     float2 s1 = cfma(k.lb16, s0, e[0]);
     float2 s2 = cfma(k.lb16, s1, e[1]);
@@ -406,7 +383,6 @@ __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)
 #endif
         }
         tmem_wait_ld();
-        if (r == 3) bu_read_done(done);
         const uint32_t o = (uint32_t)(r >> 1) * 1024u;
         const int t0 = (r & 1) * 4;
 #pragma unroll
@@ -441,8 +417,7 @@ __device__ __forceinline__ float2 pass2_full(uint32_t col0, const uint32_t (&xb)
 }
 
 // Short tile: sequential states; rows past Tc are written as zeros.
-__device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb, float2 x, int Tc,
-                                            uint64_t *done) {
+__device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8], float2 lb, float2 x, int Tc) {
 #pragma unroll 1
 #if S5_TC_REV
     for (int ch = T_TOK / 16 - 1; ch >= 0; --ch) {
@@ -470,7 +445,6 @@ __device__ __noinline__ float2 pass2_short(uint32_t col0, const uint32_t (&xb)[8
             sts32(xb[t & 7] + (uint32_t)((ch * 16 + t) >> 3) * 1024u, pv);
         }
     }
-    bu_read_done(done);
     return x;
 }
 
@@ -590,7 +564,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             for (int r = 0; r < REGIONS; ++r) {
                 mbar_init(&sb->tmem_full[r], 2);   // the commits of GEMM1's two halves
                 mbar_init(&sb->tmem_empty[r], 4);  // the four epilogue warps
-                mbar_init(&sb->p2read[r], 4);      // the four scan warps
                 mbar_init(&sb->mma2_done[r], 2);   // the commits of GEMM2's two halves
             }
             mbar_init(&sb->xready, 4);             // the four scan warps
@@ -759,15 +732,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         const float2 *slots = reinterpret_cast<const float2 *>(smem + SM_CARRY);
         const unsigned drop = sb->drop;
 
-        // Step j runs pass 1 of tile j, then pass 2 of tile j - 2.  Every exit
-        // from this loop is decided by named_bar_and, so the four warps always
-        // meet at the same barriers.
+        // Step j runs pass 1 of tile j, then pass 2 of tile j - 2.  The four
+        // warps meet only through the pipeline's mbarriers (X complete, carry
+        // slot read), each with its own count; a warp whose wait gave up leaves
+        // the loop, and the abort flag it set ends the others' next waits.
         ScanTile t0, t1, t2;
         float2 xprev = make_float2(0.f, 0.f);
         bool mine = true;
         for (int j = 0; j < n + 2; ++j) {
             if (mine && j < n) mine = scan_front(t2, j, ln, L, lane_base, kc, rec, m, tag, drop, sb, hdr);
-            if (!named_bar_and(BAR_SCAN, 128, mine)) break;
+            if (!mine) break;
             const int i = j - 2;
             if (i >= 0) {
                 // carry of tile i: from the carry warps' slot, or (one lane per
@@ -791,8 +765,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
                 if (mine) {
                     tc_fence_after();
                     const uint32_t col0 = lane_base + (uint32_t)r0 * 128u;
-                    xprev = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, carry, t0.e, &sb->p2read[r0])
-                                             : pass2_short(col0, xb, kc.lb, carry, t0.Tc, &sb->p2read[r0]);
+                    xprev = (t0.Tc == T_TOK) ? pass2_full(col0, xb, kc, carry, t0.e)
+                                             : pass2_short(col0, xb, kc.lb, carry, t0.Tc);
                     if (c0 == nchunks - 1 && args.x_last) args.x_last[(size_t)b0 * P_M + m] = xprev;
                     fence_proxy_async_smem();
                     tc_fence_before();
