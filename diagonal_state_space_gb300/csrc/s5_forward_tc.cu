@@ -197,15 +197,20 @@ __device__ __forceinline__ void st_record(float4 *p, float2 e, unsigned tag) {
 // sequences k - B*W.  W == 1: sequences k, k + G, ..., every chunk.
 struct Lane {
     int B, W, G, k, nchunks;
+    int kb, kp;   // k % B and k / B, computed once
+    __device__ __forceinline__ void init() {
+        kb = k % B;
+        kp = k / B;
+    }
     __device__ __forceinline__ bool scanner() const { return W > 1 && k >= B * W; }
     __device__ __forceinline__ int count() const {
-        if (W > 1) return scanner() ? 0 : (nchunks - k / B + W - 1) / W;
+        if (W > 1) return scanner() ? 0 : (nchunks - kp + W - 1) / W;
         return (k < B ? (B - k + G - 1) / G : 0) * nchunks;
     }
     __device__ __forceinline__ void tile(int i, int &b, int &c) const {
         if (W > 1) {
-            b = k % B;
-            c = k / B + i * W;
+            b = kb;
+            c = kp + i * W;
         } else {
             b = k + (i / nchunks) * G;
             c = i % nchunks;
@@ -538,6 +543,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
     ln.G = (int)gridDim.x;
     ln.k = (int)blockIdx.x;
     ln.nchunks = nchunks;
+    ln.init();
     const int n = ln.count();
     const bool scanner = ln.scanner();
     // the allocation must hold the 1024-aligned layout (the same for every thread)
@@ -879,7 +885,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         const float4 *carry = args.ws.carry;
         const unsigned tag_s = (sb->epoch << 2) | FLAG_INCL;
         const unsigned long long limit = sb->limit_ns;
-        const int b = ln.k % B, p = ln.k / B;
+        const int b = ln.kb, p = ln.kp;
         const size_t seq = (size_t)b * nchunks;
         bool gave_up = false;
         for (int j = 0; j < n; ++j) {
