@@ -554,8 +554,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
         griddep_wait();
         if (threadIdx.x < P_M) {
             const int m = threadIdx.x, b = ln.k - B * W;
-            const unsigned ep = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
-            const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
+            // the header's words in two independent 16-byte loads (the
+            // workspace is 16-byte aligned): epoch is word 3, the wait limit word 5
+            const uint4 h0 = __ldcg(reinterpret_cast<const uint4 *>(hdr));
+            const uint4 h1 = __ldcg(reinterpret_cast<const uint4 *>(hdr) + 1);
+            const unsigned ep = h0.w, lim = h1.y;
             const float2 S0 = args.x0 ? args.x0[(size_t)b * P_M + m] : make_float2(0.f, 0.f);
             scanner_loop(args.ws.agg + m, args.ws.carry + m, (size_t)b * nchunks, nchunks, min(RB, W), S0,
                          cpow(args.lambda_bar[m], 64), (ep << 2) | FLAG_AGG, (ep << 2) | FLAG_INCL, hdr,
@@ -585,10 +588,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
             sb->abort = 0;
             fence_mbar_init();
             griddep_wait();
-            sb->epoch = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
-            sb->drop = *reinterpret_cast<volatile unsigned *>(&hdr->drop_publish);
-            const unsigned lim = *reinterpret_cast<volatile unsigned *>(&hdr->wait_limit_us);
-            sb->limit_ns = 1000ull * (lim ? lim : 1000000u);
+            // epoch (word 3), drop_publish (4) and wait_limit_us (5) in two
+            // independent 16-byte loads instead of three ordered ones
+            const uint4 h0 = __ldcg(reinterpret_cast<const uint4 *>(hdr));
+            const uint4 h1 = __ldcg(reinterpret_cast<const uint4 *>(hdr) + 1);
+            sb->epoch = h0.w;
+            sb->drop = h1.x;
+            sb->limit_ns = 1000ull * (h1.y ? h1.y : 1000000u);
         }
         if (warp == W_TMEM) {
             tmem_alloc(&sb->tmem_base, 512);
@@ -645,10 +651,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_u, const TcArgs args) {
 #if S5_TC_REV
                 prefetch_tmap(&tmap_e);
 #endif
+                // the first u tiles come from HBM, the weight images from L2:
+                // the longer latency is requested first
+                for (int il = 0; il < n && il < STAGES; ++il) load_u(il);
                 mbar_arrive_tx(&sb->weights, BS_BYTES + CP_BYTES);
                 bulk_load(smem + SM_BS, args.ws.wimg + SM_BS, BS_BYTES, &sb->weights);
                 bulk_load(smem + SM_CP, args.ws.wimg + SM_CP, CP_BYTES, &sb->weights);
-                for (int il = 0; il < n && il < STAGES; ++il) load_u(il);
             }
             ok = n == 0 || pipe_wait(&sb->weights, 0, sb, hdr);
             if (warp < 2) {
