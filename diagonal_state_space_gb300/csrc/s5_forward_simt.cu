@@ -39,7 +39,9 @@ struct SimtSmem {
     size_t u_off, x_off, a_off, w_off, seg_off, tagg_off, carry_off, g_off, total;
 };
 
-__host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, bool varying) {
+// res: B_bar^T [H][Pe] and C~^T [P][He] stay in shared memory for the CTA's
+// lifetime instead of being staged in chunks of SIMT_KC features per tile.
+__host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, bool varying, bool res = false) {
     SimtSmem s;
     s.T = T;
     s.Pe = P + (P & 1);
@@ -49,7 +51,8 @@ __host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, boo
     s.u_off = take(sizeof(float) * (size_t)T * H);
     s.x_off = take(sizeof(float2) * (size_t)T * s.Pe);
     s.a_off = take(varying ? sizeof(float2) * (size_t)T * s.Pe : 0);
-    s.w_off = take(sizeof(float2) * (size_t)SIMT_KC * (s.Pe > s.He ? s.Pe : s.He));
+    s.w_off = take(res ? sizeof(float2) * ((size_t)H * s.Pe + (size_t)P * s.He)
+                       : sizeof(float2) * (size_t)SIMT_KC * (s.Pe > s.He ? s.Pe : s.He));
     s.seg_off = take(sizeof(float4) * (size_t)nseg * P);
     s.tagg_off = take(sizeof(float4) * (size_t)P);
     s.carry_off = take(sizeof(float4) * (size_t)P);
@@ -96,8 +99,11 @@ __device__ __forceinline__ void irregular_step(const ModeConst &m, float2 inv_la
     gain = cmul(am1, inv_lam);
 }
 
-template <typename UT, typename YT, bool VARYING>
-__global__ void __launch_bounds__(SIMT_THREADS)
+// NT threads per CTA; RES: the weights stay resident in shared memory (loaded
+// once per CTA, transposed), so the projection loops run without staging,
+// barriers or L2 round trips.
+template <typename UT, typename YT, bool VARYING, bool RES, int NT>
+__global__ void __launch_bounds__(NT)
 fwd_simt_kernel(const SimtArgs args) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ long long s_tile;
@@ -108,12 +114,14 @@ fwd_simt_kernel(const SimtArgs args) {
 
     const int tid = threadIdx.x;
     const int B = args.B, L = args.L, H = args.H, P = args.P, T = args.T, nseg = args.nseg;
-    const SimtSmem lay = simt_smem(T, H, P, nseg, VARYING);
+    const SimtSmem lay = simt_smem(T, H, P, nseg, VARYING, RES);
     const int Pe = lay.Pe, He = lay.He;
     float *u_s = reinterpret_cast<float *>(smem + lay.u_off);
     float2 *x_s = reinterpret_cast<float2 *>(smem + lay.x_off);
     float2 *a_s = reinterpret_cast<float2 *>(smem + lay.a_off);
     float2 *w_s = reinterpret_cast<float2 *>(smem + lay.w_off);
+    // resident copies (RES): B_bar^T [H][Pe], C~^T [P][He]
+    float2 *wres = w_s, *cres = w_s + (size_t)H * Pe;
     float4 *seg_s = reinterpret_cast<float4 *>(smem + lay.seg_off);
     float4 *tagg_s = reinterpret_cast<float4 *>(smem + lay.tagg_off);
     float4 *carry_s = reinterpret_cast<float4 *>(smem + lay.carry_off);
@@ -131,6 +139,18 @@ fwd_simt_kernel(const SimtArgs args) {
     YT *y = static_cast<YT *>(args.y);
     const int PQ = (P + 1) / 2, HQ = (H + 3) / 4;
     const int nmt1 = (T / 4) * PQ, nmt2 = (T / 4) * HQ;
+    if (RES) {
+        // the weights, once per CTA (the first barrier of the tile loop
+        // orders these stores before any read)
+        for (int i = tid; i < H * Pe; i += NT) {
+            const int kk = i / Pe, p = i - kk * Pe;
+            wres[i] = p < P ? args.w[(size_t)p * H + kk] : make_float2(0.f, 0.f);
+        }
+        for (int i = tid; i < P * He; i += NT) {
+            const int q = i / He, h = i - q * He;
+            cres[i] = h < H ? args.c_tilde[(size_t)h * P + q] : make_float2(0.f, 0.f);
+        }
+    }
 
     for (;;) {
         __syncthreads();
@@ -147,12 +167,12 @@ fwd_simt_kernel(const SimtArgs args) {
 
         // 1. input tile (zero rows past the ragged end)
         const size_t row0 = (size_t)b * L + t0;
-        for (int i = tid; i < T * H; i += SIMT_THREADS) {
+        for (int i = tid; i < T * H; i += NT) {
             int t = i / H, h = i - t * H;
             u_s[i] = t < Tc ? load_elem<UT>(u + (row0 + t) * H + h) : 0.f;
         }
         if (VARYING) {
-            for (int t = tid; t < T; t += SIMT_THREADS) {
+            for (int t = tid; t < T; t += NT) {
                 float gv = 0.f;
                 if (t < Tc) {
                     gv = __ldg(args.g + row0 + t);
@@ -171,22 +191,26 @@ fwd_simt_kernel(const SimtArgs args) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
+            if (RES) __syncthreads();   // the u tile is complete
             for (int h0 = 0; h0 < H; h0 += SIMT_KC) {
                 const int kc = min(SIMT_KC, H - h0);
-                __syncthreads();
-                for (int i = tid; i < Pe * SIMT_KC; i += SIMT_THREADS) {
-                    int p = i / SIMT_KC, kk = i - p * SIMT_KC;
-                    w_s[kk * Pe + p] = (p < P && kk < kc) ? args.w[(size_t)p * H + h0 + kk]
-                                                         : make_float2(0.f, 0.f);
+                if (!RES) {
+                    __syncthreads();
+                    for (int i = tid; i < Pe * SIMT_KC; i += NT) {
+                        int p = i / SIMT_KC, kk = i - p * SIMT_KC;
+                        w_s[kk * Pe + p] = (p < P && kk < kc) ? args.w[(size_t)p * H + h0 + kk]
+                                                             : make_float2(0.f, 0.f);
+                    }
+                    __syncthreads();
                 }
-                __syncthreads();
+                const float2 *wk = RES ? wres + (size_t)h0 * Pe : w_s;
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
-                    const int mt = tid + m * SIMT_THREADS;
+                    const int mt = tid + m * NT;
                     if (mt < nmt1) {
                         const int pq = mt % PQ, tq = mt / PQ;
                         const float *ur = u_s + (size_t)(4 * tq) * H + h0;
-                        const float4 *wr = reinterpret_cast<const float4 *>(w_s + 2 * pq);
+                        const float4 *wr = reinterpret_cast<const float4 *>(wk + 2 * pq);
                         for (int kk = 0; kk < kc; ++kk) {
                             float4 wv = wr[kk * (Pe / 2)];
 #pragma unroll
@@ -203,7 +227,7 @@ fwd_simt_kernel(const SimtArgs args) {
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
-                const int mt = tid + m * SIMT_THREADS;
+                const int mt = tid + m * NT;
                 if (mt < nmt1) {
                     const int pq = mt % PQ, tq = mt / PQ;
 #pragma unroll
@@ -217,7 +241,7 @@ fwd_simt_kernel(const SimtArgs args) {
 
         // 3. per-segment fold, from a zero start
         const int seglen = (Tc + nseg - 1) / nseg;
-        for (int i = tid; i < P * nseg; i += SIMT_THREADS) {
+        for (int i = tid; i < P * nseg; i += NT) {
             const int p = i % P, s = i / P;
             const int s0 = min(Tc, s * seglen), s1 = min(Tc, s0 + seglen);
             float2 A = make_float2(1.f, 0.f), E = make_float2(0.f, 0.f);
@@ -246,7 +270,7 @@ fwd_simt_kernel(const SimtArgs args) {
         __syncthreads();
 
         // 4. tile aggregate, publication and look-back
-        for (int p = tid; p < P; p += SIMT_THREADS) {
+        for (int p = tid; p < P; p += NT) {
             float2 A = make_float2(1.f, 0.f), E = make_float2(0.f, 0.f);
             for (int s = 0; s < nseg; ++s) {
                 const float4 v = seg_s[(size_t)s * P + p];
@@ -285,7 +309,7 @@ fwd_simt_kernel(const SimtArgs args) {
                 }
                 __syncthreads();
                 const int n = s_n;
-                for (int p = tid; p < P; p += SIMT_THREADS) {
+                for (int p = tid; p < P; p += NT) {
                     float4 cs = carry_s[p];
                     float2 mult = make_float2(cs.x, cs.y), accv = make_float2(cs.z, cs.w);
                     for (int l0 = 0; l0 < n; l0 += 8) {
@@ -320,7 +344,7 @@ fwd_simt_kernel(const SimtArgs args) {
                 if (s_stop) break;
             }
         }
-        for (int p = tid; p < P; p += SIMT_THREADS) {
+        for (int p = tid; p < P; p += NT) {
             const float4 ta = tagg_s[p];
             const float4 cs = carry_s[p];
             const float2 inc = cfma(make_float2(ta.x, ta.y), make_float2(cs.z, cs.w),
@@ -335,7 +359,7 @@ fwd_simt_kernel(const SimtArgs args) {
         }
 
         // 5. rerun every segment from its true carry, x_k in place of b_k
-        for (int i = tid; i < P * nseg; i += SIMT_THREADS) {
+        for (int i = tid; i < P * nseg; i += NT) {
             const int p = i % P, s = i / P;
             const int s0 = min(Tc, s * seglen), s1 = min(Tc, s0 + seglen);
             const float4 cs = carry_s[p];
@@ -369,22 +393,26 @@ fwd_simt_kernel(const SimtArgs args) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
+            if (RES) __syncthreads();   // x is complete
             for (int q0 = 0; q0 < P; q0 += SIMT_KC) {
                 const int kc = min(SIMT_KC, P - q0);
-                __syncthreads();
-                for (int i = tid; i < He * SIMT_KC; i += SIMT_THREADS) {
-                    int h = i / SIMT_KC, kk = i - h * SIMT_KC;
-                    w_s[kk * He + h] = (h < H && kk < kc) ? args.c_tilde[(size_t)h * P + q0 + kk]
-                                                         : make_float2(0.f, 0.f);
+                if (!RES) {
+                    __syncthreads();
+                    for (int i = tid; i < He * SIMT_KC; i += NT) {
+                        int h = i / SIMT_KC, kk = i - h * SIMT_KC;
+                        w_s[kk * He + h] = (h < H && kk < kc) ? args.c_tilde[(size_t)h * P + q0 + kk]
+                                                             : make_float2(0.f, 0.f);
+                    }
+                    __syncthreads();
                 }
-                __syncthreads();
+                const float2 *ck = RES ? cres + (size_t)q0 * He : w_s;
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
-                    const int mt = tid + m * SIMT_THREADS;
+                    const int mt = tid + m * NT;
                     if (mt < nmt2) {
                         const int hq = mt % HQ, tq = mt / HQ;
                         const float2 *xr = x_s + (size_t)(4 * tq) * Pe + q0;
-                        const float4 *cr = reinterpret_cast<const float4 *>(w_s + 4 * hq);
+                        const float4 *cr = reinterpret_cast<const float4 *>(ck + 4 * hq);
                         for (int kk = 0; kk < kc; ++kk) {
                             const float4 c01 = cr[kk * (He / 2)];
                             const float4 c23 = cr[kk * (He / 2) + 1];
@@ -402,7 +430,7 @@ fwd_simt_kernel(const SimtArgs args) {
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
-                const int mt = tid + m * SIMT_THREADS;
+                const int mt = tid + m * NT;
                 if (mt < nmt2) {
                     const int hq = mt % HQ, tq = mt / HQ;
 #pragma unroll
@@ -459,20 +487,32 @@ int simt_tile_tokens(int H, int P, bool varying) {
     return 0;
 }
 
-template <typename UT, typename YT, bool V>
-static cudaError_t launch_t(const SimtArgs &a, cudaStream_t st, int num_sms) {
-    const size_t smem = simt_smem(a.T, a.H, a.P, a.nseg, V).total;
-    auto kern = fwd_simt_kernel<UT, YT, V>;
+constexpr int SIMT_RES_THREADS = 512;
+constexpr size_t SIMT_RES_SMEM_MAX = 220 * 1024;   // one CTA per SM
+
+template <typename UT, typename YT, bool V, bool RES, int NT>
+static cudaError_t launch_k(const SimtArgs &a, cudaStream_t st, int num_sms) {
+    const size_t smem = simt_smem(a.T, a.H, a.P, a.nseg, V, RES).total;
+    auto kern = fwd_simt_kernel<UT, YT, V, RES, NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SIMT_THREADS, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     long long grid = (long long)per_sm * num_sms;
     if (grid > a.ntiles) grid = a.ntiles;
-    kern<<<(unsigned)grid, SIMT_THREADS, smem, st>>>(a);
+    kern<<<(unsigned)grid, NT, smem, st>>>(a);
     return cudaGetLastError();
+}
+
+// Weights resident in shared memory whenever they fit beside the tile
+// buffers (one CTA of 512 threads per SM); else staged per tile.
+template <typename UT, typename YT, bool V>
+static cudaError_t launch_t(const SimtArgs &a, cudaStream_t st, int num_sms) {
+    if (simt_smem(a.T, a.H, a.P, a.nseg, V, true).total <= SIMT_RES_SMEM_MAX)
+        return launch_k<UT, YT, V, true, SIMT_RES_THREADS>(a, st, num_sms);
+    return launch_k<UT, YT, V, false, SIMT_THREADS>(a, st, num_sms);
 }
 
 cudaError_t launch_forward_simt(const SimtArgs &a, bool u_bf16, bool y_bf16, bool varying,
