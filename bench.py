@@ -783,24 +783,54 @@ def run_stack(args):
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, dist)
     tokens = w.B * w.L
-    # end to end: u0 and G from pinned host memory, du0 back
+    # end to end: u0 and G from pinned host memory, du0 back, every step.  Two
+    # device sets and two copy streams let step i's copies overlap step
+    # i-1's compute (du0 is staged on the device so that the next step's
+    # backward may overwrite the stack's own buffer).
     u_host = torch.from_numpy(np.ascontiguousarray(inp["u0"])).pin_memory()
     g_host = torch.from_numpy(np.ascontiguousarray(inp["G"])).pin_memory()
-    du_host = torch.empty(u_host.shape, dtype=torch.float32).pin_memory()
+    du_hosts = [torch.empty(u_host.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    u_in, g_in = [u0, torch.empty_like(u0)], [G, torch.empty_like(G)]
+    du_stage = [torch.empty_like(st.ubar) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
-        u0.copy_(u_host, non_blocking=True)
-        G.copy_(g_host, non_blocking=True)
-        step()
-        du_host.copy_(st.ubar, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if used[k]:
+                s_in.wait_event(ev_cmp[k])      # step i-2 has consumed set k
+            u_in[k].copy_(u_host, non_blocking=True)
+            g_in[k].copy_(g_host, non_blocking=True)
+            ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        if used[k]:
+            stream.wait_event(ev_out[k])        # du0 of step i-2 has been read back
+        st.forward(u_in[k])
+        st.backward(g_in[k])
+        du_stage[k].copy_(st.ubar)
+        ev_cmp[k].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[k])
+            du_hosts[k].copy_(du_stage[k], non_blocking=True)
+            ev_out[k].record(s_out)
+        used[k] = True
 
     e2e_steps = max(1, min(args.e2e_steps, 5))
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(a0)
+    s_out.wait_event(a0)
+    for i in range(2, 2 + e2e_steps):
+        e2e_step(i)
+    for ev in ev_out:
+        stream.wait_event(ev)
     a1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
@@ -829,7 +859,7 @@ def run_stack(args):
                      "peak_source": "%s (MEASURED_PEAKS.json bf16_tflops)" % peak_kind,
                      "flops_per_step": flops, "traffic": None},
         "e2e": {"value": job_throughput(tokens, world, e2e_ms), "unit": "tokens/s",
-                "h2d_bytes_per_step": 2 * u_host.numel() * 4, "d2h_bytes_per_step": du_host.numel() * 4,
+                "h2d_bytes_per_step": 2 * u_host.numel() * 4, "d2h_bytes_per_step": du_hosts[0].numel() * 4,
                 "ms_per_step": e2e_ms},
         # per step one discretize of all layers' modes; per layer: forward weights,
         # LayerNorm, scan aggregates + apply, gate pre/post; backward gate pre/post,
