@@ -34,6 +34,20 @@ constexpr float TWO_PI_1 = 0x1.fb5444p-10f;
 constexpr float TWO_PI_2 = 0x1.68c234p-37f;
 constexpr float INV_TWO_PI = 0.15915494f;
 
+// Per-thread asynchronous copies (8 bytes) into shared memory: the staged
+// weights of the next chunk load while the current chunk is computed.
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 struct SimtSmem {
     int Pe, He, T;
     size_t u_off, x_off, a_off, w_off, seg_off, tagg_off, carry_off, g_off, total;
@@ -52,7 +66,7 @@ __host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, boo
     s.x_off = take(sizeof(float2) * (size_t)T * s.Pe);
     s.a_off = take(varying ? sizeof(float2) * (size_t)T * s.Pe : 0);
     s.w_off = take(res ? sizeof(float2) * ((size_t)H * s.Pe + (size_t)P * s.He)
-                       : sizeof(float2) * (size_t)SIMT_KC * (s.Pe > s.He ? s.Pe : s.He));
+                       : 2 * sizeof(float2) * (size_t)SIMT_KC * ((s.Pe > s.He ? s.Pe : s.He) + 2));
     s.seg_off = take(sizeof(float4) * (size_t)nseg * P);
     s.tagg_off = take(sizeof(float4) * (size_t)P);
     s.carry_off = take(sizeof(float4) * (size_t)P);
@@ -122,6 +136,38 @@ fwd_simt_kernel(const SimtArgs args) {
     float2 *w_s = reinterpret_cast<float2 *>(smem + lay.w_off);
     // resident copies (RES): B_bar^T [H][Pe], C~^T [P][He]
     float2 *wres = w_s, *cres = w_s + (size_t)H * Pe;
+    // staged chunks (!RES): two buffers of SIMT_KC rows, refilled alternately
+    // staged rows are padded by two float2: rows kk and kk+1 then start four
+    // banks apart, so the transposing stores of a warp's 16 row indices meet
+    // in pairs, not all in one bank, and rows stay 16-byte aligned
+    const int PeS = Pe + 2, HeS = He + 2;
+    const size_t wbuf_len = (size_t)SIMT_KC * ((Pe > He ? Pe : He) + 2);
+    auto wbuf = [&](int k) { return w_s + (size_t)(k & 1) * wbuf_len; };
+    // chunk [h0, h0 + SIMT_KC) of B_bar^T (rows kk, columns p) or C~^T
+    auto stage_w = [&](float2 *dst, int h0) {
+        const int kc = min(SIMT_KC, H - h0);
+        for (int i = tid; i < Pe * SIMT_KC; i += NT) {
+            const int p = i / SIMT_KC, kk = i - p * SIMT_KC;
+            float2 *d = dst + kk * PeS + p;
+            if (p < P && kk < kc)
+                cp_async8(d, args.w + (size_t)p * H + h0 + kk);
+            else
+                *d = make_float2(0.f, 0.f);
+        }
+        cp_async_commit();
+    };
+    auto stage_c = [&](float2 *dst, int q0) {
+        const int kc = min(SIMT_KC, P - q0);
+        for (int i = tid; i < He * SIMT_KC; i += NT) {
+            const int h = i / SIMT_KC, kk = i - h * SIMT_KC;
+            float2 *d = dst + kk * HeS + h;
+            if (h < H && kk < kc)
+                cp_async8(d, args.c_tilde + (size_t)h * P + q0 + kk);
+            else
+                *d = make_float2(0.f, 0.f);
+        }
+        cp_async_commit();
+    };
     float4 *seg_s = reinterpret_cast<float4 *>(smem + lay.seg_off);
     float4 *tagg_s = reinterpret_cast<float4 *>(smem + lay.tagg_off);
     float4 *carry_s = reinterpret_cast<float4 *>(smem + lay.carry_off);
@@ -165,6 +211,10 @@ fwd_simt_kernel(const SimtArgs args) {
         const int t0 = c * T;
         const int Tc = min(T, L - t0);
 
+        // the first weight chunk loads while the u tile does (the barriers at
+        // the loop top follow every read of the buffers by the tile before)
+        if (!RES) stage_w(wbuf(0), 0);
+
         // 1. input tile (zero rows past the ragged end)
         const size_t row0 = (size_t)b * L + t0;
         for (int i = tid; i < T * H; i += NT) {
@@ -192,18 +242,21 @@ fwd_simt_kernel(const SimtArgs args) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
             if (RES) __syncthreads();   // the u tile is complete
-            for (int h0 = 0; h0 < H; h0 += SIMT_KC) {
+            for (int h0 = 0, ci = 0; h0 < H; h0 += SIMT_KC, ++ci) {
                 const int kc = min(SIMT_KC, H - h0);
                 if (!RES) {
-                    __syncthreads();
-                    for (int i = tid; i < Pe * SIMT_KC; i += NT) {
-                        int p = i / SIMT_KC, kk = i - p * SIMT_KC;
-                        w_s[kk * Pe + p] = (p < P && kk < kc) ? args.w[(size_t)p * H + h0 + kk]
-                                                             : make_float2(0.f, 0.f);
+                    // chunk ci+1 into the other buffer (read two chunks ago,
+                    // released by the barrier ending that chunk), then chunk ci
+                    if (h0 + SIMT_KC < H) {
+                        stage_w(wbuf(ci + 1), h0 + SIMT_KC);
+                        cp_async_wait<1>();
+                    } else {
+                        cp_async_wait<0>();
                     }
                     __syncthreads();
                 }
-                const float2 *wk = RES ? wres + (size_t)h0 * Pe : w_s;
+                const float2 *wk = RES ? wres + (size_t)h0 * Pe : wbuf(ci);
+                const int wstride = RES ? Pe : PeS;   // float2 per staged row
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
                     const int mt = tid + m * NT;
@@ -212,7 +265,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         const float *ur = u_s + (size_t)(4 * tq) * H + h0;
                         const float4 *wr = reinterpret_cast<const float4 *>(wk + 2 * pq);
                         for (int kk = 0; kk < kc; ++kk) {
-                            float4 wv = wr[kk * (Pe / 2)];
+                            float4 wv = wr[kk * (wstride / 2)];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 float uv = ur[i * H + kk];
@@ -224,6 +277,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         }
                     }
                 }
+                if (!RES) __syncthreads();   // every thread is done with this chunk's buffer
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
@@ -238,6 +292,8 @@ fwd_simt_kernel(const SimtArgs args) {
             }
         }
         __syncthreads();
+        // the readout's first weight chunk loads during the scan
+        if (!RES) stage_c(wbuf(0), 0);
 
         // 3. per-segment fold, from a zero start
         const int seglen = (Tc + nseg - 1) / nseg;
@@ -394,18 +450,19 @@ fwd_simt_kernel(const SimtArgs args) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
             if (RES) __syncthreads();   // x is complete
-            for (int q0 = 0; q0 < P; q0 += SIMT_KC) {
+            for (int q0 = 0, ci = 0; q0 < P; q0 += SIMT_KC, ++ci) {
                 const int kc = min(SIMT_KC, P - q0);
                 if (!RES) {
-                    __syncthreads();
-                    for (int i = tid; i < He * SIMT_KC; i += NT) {
-                        int h = i / SIMT_KC, kk = i - h * SIMT_KC;
-                        w_s[kk * He + h] = (h < H && kk < kc) ? args.c_tilde[(size_t)h * P + q0 + kk]
-                                                             : make_float2(0.f, 0.f);
+                    if (q0 + SIMT_KC < P) {
+                        stage_c(wbuf(ci + 1), q0 + SIMT_KC);
+                        cp_async_wait<1>();
+                    } else {
+                        cp_async_wait<0>();
                     }
-                    __syncthreads();
+                    __syncthreads();   // also: x is complete
                 }
-                const float2 *ck = RES ? cres + (size_t)q0 * He : w_s;
+                const float2 *ck = RES ? cres + (size_t)q0 * He : wbuf(ci);
+                const int cstride = RES ? He : HeS;   // float2 per staged row
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
                     const int mt = tid + m * NT;
@@ -414,8 +471,8 @@ fwd_simt_kernel(const SimtArgs args) {
                         const float2 *xr = x_s + (size_t)(4 * tq) * Pe + q0;
                         const float4 *cr = reinterpret_cast<const float4 *>(ck + 4 * hq);
                         for (int kk = 0; kk < kc; ++kk) {
-                            const float4 c01 = cr[kk * (He / 2)];
-                            const float4 c23 = cr[kk * (He / 2) + 1];
+                            const float4 c01 = cr[kk * (cstride / 2)];
+                            const float4 c23 = cr[kk * (cstride / 2) + 1];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 xv = xr[(size_t)i * Pe + kk];
@@ -427,6 +484,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         }
                     }
                 }
+                if (!RES) __syncthreads();   // every thread is done with this chunk's buffer
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
@@ -481,7 +539,7 @@ int simt_tile_tokens(int H, int P, bool varying) {
     for (int T = 64; T >= 4; T /= 2) {
         if ((T / 4) * PQ > SIMT_MAXMT * SIMT_THREADS) continue;
         if ((T / 4) * HQ > SIMT_MAXMT * SIMT_THREADS) continue;
-        if (simt_smem(T, H, P, simt_nseg(P), varying).total > 200 * 1024) continue;
+        if (simt_smem(T, H, P, simt_nseg(P), varying).total > 220 * 1024) continue;
         return T;
     }
     return 0;
@@ -512,6 +570,9 @@ template <typename UT, typename YT, bool V>
 static cudaError_t launch_t(const SimtArgs &a, cudaStream_t st, int num_sms) {
     if (simt_smem(a.T, a.H, a.P, a.nseg, V, true).total <= SIMT_RES_SMEM_MAX)
         return launch_k<UT, YT, V, true, SIMT_RES_THREADS>(a, st, num_sms);
+    // staged weights: twice the warps when a single CTA fills an SM's shared memory
+    if (simt_smem(a.T, a.H, a.P, a.nseg, V, false).total > 112 * 1024)
+        return launch_k<UT, YT, V, false, SIMT_RES_THREADS>(a, st, num_sms);
     return launch_k<UT, YT, V, false, SIMT_THREADS>(a, st, num_sms);
 }
 
