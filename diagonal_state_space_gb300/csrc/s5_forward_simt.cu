@@ -53,9 +53,7 @@ struct SimtSmem {
     size_t u_off, x_off, a_off, w_off, seg_off, tagg_off, carry_off, g_off, total;
 };
 
-// res: B_bar^T [H][Pe] and C~^T [P][He] stay in shared memory for the CTA's
-// lifetime instead of being staged in chunks of SIMT_KC features per tile.
-__host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, bool varying, bool res = false) {
+__host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, bool varying) {
     SimtSmem s;
     s.T = T;
     s.Pe = P + (P & 1);
@@ -65,8 +63,8 @@ __host__ __device__ inline SimtSmem simt_smem(int T, int H, int P, int nseg, boo
     s.u_off = take(sizeof(float) * (size_t)T * H);
     s.x_off = take(sizeof(float2) * (size_t)T * s.Pe);
     s.a_off = take(varying ? sizeof(float2) * (size_t)T * s.Pe : 0);
-    s.w_off = take(res ? sizeof(float2) * ((size_t)H * s.Pe + (size_t)P * s.He)
-                       : 2 * sizeof(float2) * (size_t)SIMT_KC * ((s.Pe > s.He ? s.Pe : s.He) + 2));
+    // two staged chunks of SIMT_KC weight rows, each row padded by two float2
+    s.w_off = take(2 * sizeof(float2) * (size_t)SIMT_KC * ((s.Pe > s.He ? s.Pe : s.He) + 2));
     s.seg_off = take(sizeof(float4) * (size_t)nseg * P);
     s.tagg_off = take(sizeof(float4) * (size_t)P);
     s.carry_off = take(sizeof(float4) * (size_t)P);
@@ -113,10 +111,8 @@ __device__ __forceinline__ void irregular_step(const ModeConst &m, float2 inv_la
     gain = cmul(am1, inv_lam);
 }
 
-// NT threads per CTA; RES: the weights stay resident in shared memory (loaded
-// once per CTA, transposed), so the projection loops run without staging,
-// barriers or L2 round trips.
-template <typename UT, typename YT, bool VARYING, bool RES, int NT>
+// NT threads per CTA.
+template <typename UT, typename YT, bool VARYING, int NT>
 __global__ void __launch_bounds__(NT)
 fwd_simt_kernel(const SimtArgs args) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -128,15 +124,13 @@ fwd_simt_kernel(const SimtArgs args) {
 
     const int tid = threadIdx.x;
     const int B = args.B, L = args.L, H = args.H, P = args.P, T = args.T, nseg = args.nseg;
-    const SimtSmem lay = simt_smem(T, H, P, nseg, VARYING, RES);
+    const SimtSmem lay = simt_smem(T, H, P, nseg, VARYING);
     const int Pe = lay.Pe, He = lay.He;
     float *u_s = reinterpret_cast<float *>(smem + lay.u_off);
     float2 *x_s = reinterpret_cast<float2 *>(smem + lay.x_off);
     float2 *a_s = reinterpret_cast<float2 *>(smem + lay.a_off);
     float2 *w_s = reinterpret_cast<float2 *>(smem + lay.w_off);
-    // resident copies (RES): B_bar^T [H][Pe], C~^T [P][He]
-    float2 *wres = w_s, *cres = w_s + (size_t)H * Pe;
-    // staged chunks (!RES): two buffers of SIMT_KC rows, refilled alternately
+    // staged chunks: two buffers of SIMT_KC rows, refilled alternately
     // staged rows are padded by two float2: rows kk and kk+1 then start four
     // banks apart, so the transposing stores of a warp's 16 row indices meet
     // in pairs, not all in one bank, and rows stay 16-byte aligned
@@ -185,18 +179,6 @@ fwd_simt_kernel(const SimtArgs args) {
     YT *y = static_cast<YT *>(args.y);
     const int PQ = (P + 1) / 2, HQ = (H + 3) / 4;
     const int nmt1 = (T / 4) * PQ, nmt2 = (T / 4) * HQ;
-    if (RES) {
-        // the weights, once per CTA (the first barrier of the tile loop
-        // orders these stores before any read)
-        for (int i = tid; i < H * Pe; i += NT) {
-            const int kk = i / Pe, p = i - kk * Pe;
-            wres[i] = p < P ? args.w[(size_t)p * H + kk] : make_float2(0.f, 0.f);
-        }
-        for (int i = tid; i < P * He; i += NT) {
-            const int q = i / He, h = i - q * He;
-            cres[i] = h < H ? args.c_tilde[(size_t)h * P + q] : make_float2(0.f, 0.f);
-        }
-    }
 
     for (;;) {
         __syncthreads();
@@ -213,7 +195,7 @@ fwd_simt_kernel(const SimtArgs args) {
 
         // the first weight chunk loads while the u tile does (the barriers at
         // the loop top follow every read of the buffers by the tile before)
-        if (!RES) stage_w(wbuf(0), 0);
+        stage_w(wbuf(0), 0);
 
         // 1. input tile (zero rows past the ragged end)
         const size_t row0 = (size_t)b * L + t0;
@@ -241,22 +223,18 @@ fwd_simt_kernel(const SimtArgs args) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
-            if (RES) __syncthreads();   // the u tile is complete
             for (int h0 = 0, ci = 0; h0 < H; h0 += SIMT_KC, ++ci) {
                 const int kc = min(SIMT_KC, H - h0);
-                if (!RES) {
-                    // chunk ci+1 into the other buffer (read two chunks ago,
-                    // released by the barrier ending that chunk), then chunk ci
-                    if (h0 + SIMT_KC < H) {
-                        stage_w(wbuf(ci + 1), h0 + SIMT_KC);
-                        cp_async_wait<1>();
-                    } else {
-                        cp_async_wait<0>();
-                    }
-                    __syncthreads();
+                // chunk ci+1 into the other buffer (read two chunks ago,
+                // released by the barrier ending that chunk), then chunk ci
+                if (h0 + SIMT_KC < H) {
+                    stage_w(wbuf(ci + 1), h0 + SIMT_KC);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
                 }
-                const float2 *wk = RES ? wres + (size_t)h0 * Pe : wbuf(ci);
-                const int wstride = RES ? Pe : PeS;   // float2 per staged row
+                __syncthreads();   // chunk ci (and, the first time, the u tile) is complete
+                const float2 *wk = wbuf(ci);
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
                     const int mt = tid + m * NT;
@@ -265,7 +243,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         const float *ur = u_s + (size_t)(4 * tq) * H + h0;
                         const float4 *wr = reinterpret_cast<const float4 *>(wk + 2 * pq);
                         for (int kk = 0; kk < kc; ++kk) {
-                            float4 wv = wr[kk * (wstride / 2)];
+                            float4 wv = wr[kk * (PeS / 2)];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 float uv = ur[i * H + kk];
@@ -277,7 +255,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         }
                     }
                 }
-                if (!RES) __syncthreads();   // every thread is done with this chunk's buffer
+                __syncthreads();   // every thread is done with this chunk's buffer
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
@@ -293,7 +271,7 @@ fwd_simt_kernel(const SimtArgs args) {
         }
         __syncthreads();
         // the readout's first weight chunk loads during the scan
-        if (!RES) stage_c(wbuf(0), 0);
+        stage_c(wbuf(0), 0);
 
         // 3. per-segment fold, from a zero start
         const int seglen = (Tc + nseg - 1) / nseg;
@@ -449,20 +427,16 @@ fwd_simt_kernel(const SimtArgs args) {
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[m][i][j] = 0.f;
-            if (RES) __syncthreads();   // x is complete
             for (int q0 = 0, ci = 0; q0 < P; q0 += SIMT_KC, ++ci) {
                 const int kc = min(SIMT_KC, P - q0);
-                if (!RES) {
-                    if (q0 + SIMT_KC < P) {
-                        stage_c(wbuf(ci + 1), q0 + SIMT_KC);
-                        cp_async_wait<1>();
-                    } else {
-                        cp_async_wait<0>();
-                    }
-                    __syncthreads();   // also: x is complete
+                if (q0 + SIMT_KC < P) {
+                    stage_c(wbuf(ci + 1), q0 + SIMT_KC);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
                 }
-                const float2 *ck = RES ? cres + (size_t)q0 * He : wbuf(ci);
-                const int cstride = RES ? He : HeS;   // float2 per staged row
+                __syncthreads();   // chunk ci (and, the first time, x) is complete
+                const float2 *ck = wbuf(ci);
 #pragma unroll
                 for (int m = 0; m < SIMT_MAXMT; ++m) {
                     const int mt = tid + m * NT;
@@ -471,8 +445,8 @@ fwd_simt_kernel(const SimtArgs args) {
                         const float2 *xr = x_s + (size_t)(4 * tq) * Pe + q0;
                         const float4 *cr = reinterpret_cast<const float4 *>(ck + 4 * hq);
                         for (int kk = 0; kk < kc; ++kk) {
-                            const float4 c01 = cr[kk * (cstride / 2)];
-                            const float4 c23 = cr[kk * (cstride / 2) + 1];
+                            const float4 c01 = cr[kk * (HeS / 2)];
+                            const float4 c23 = cr[kk * (HeS / 2) + 1];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const float2 xv = xr[(size_t)i * Pe + kk];
@@ -484,7 +458,7 @@ fwd_simt_kernel(const SimtArgs args) {
                         }
                     }
                 }
-                if (!RES) __syncthreads();   // every thread is done with this chunk's buffer
+                __syncthreads();   // every thread is done with this chunk's buffer
             }
 #pragma unroll
             for (int m = 0; m < SIMT_MAXMT; ++m) {
@@ -545,13 +519,12 @@ int simt_tile_tokens(int H, int P, bool varying) {
     return 0;
 }
 
-constexpr int SIMT_RES_THREADS = 512;
-constexpr size_t SIMT_RES_SMEM_MAX = 220 * 1024;   // one CTA per SM
+constexpr int SIMT_BIG_THREADS = 512;
 
-template <typename UT, typename YT, bool V, bool RES, int NT>
+template <typename UT, typename YT, bool V, int NT>
 static cudaError_t launch_k(const SimtArgs &a, cudaStream_t st, int num_sms) {
-    const size_t smem = simt_smem(a.T, a.H, a.P, a.nseg, V, RES).total;
-    auto kern = fwd_simt_kernel<UT, YT, V, RES, NT>;
+    const size_t smem = simt_smem(a.T, a.H, a.P, a.nseg, V).total;
+    auto kern = fwd_simt_kernel<UT, YT, V, NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -564,16 +537,12 @@ static cudaError_t launch_k(const SimtArgs &a, cudaStream_t st, int num_sms) {
     return cudaGetLastError();
 }
 
-// Weights resident in shared memory whenever they fit beside the tile
-// buffers (one CTA of 512 threads per SM); else staged per tile.
+// Twice the warps when a single CTA fills an SM's shared memory.
 template <typename UT, typename YT, bool V>
 static cudaError_t launch_t(const SimtArgs &a, cudaStream_t st, int num_sms) {
-    if (simt_smem(a.T, a.H, a.P, a.nseg, V, true).total <= SIMT_RES_SMEM_MAX)
-        return launch_k<UT, YT, V, true, SIMT_RES_THREADS>(a, st, num_sms);
-    // staged weights: twice the warps when a single CTA fills an SM's shared memory
-    if (simt_smem(a.T, a.H, a.P, a.nseg, V, false).total > 112 * 1024)
-        return launch_k<UT, YT, V, false, SIMT_RES_THREADS>(a, st, num_sms);
-    return launch_k<UT, YT, V, false, SIMT_THREADS>(a, st, num_sms);
+    if (simt_smem(a.T, a.H, a.P, a.nseg, V).total > 112 * 1024)
+        return launch_k<UT, YT, V, SIMT_BIG_THREADS>(a, st, num_sms);
+    return launch_k<UT, YT, V, SIMT_THREADS>(a, st, num_sms);
 }
 
 cudaError_t launch_forward_simt(const SimtArgs &a, bool u_bf16, bool y_bf16, bool varying,
