@@ -65,7 +65,11 @@ typedef enum { S5_ZOH = 0, S5_BILINEAR = 1 } s5_discretization;
  *   lambda_bar_n = exp(lambda_n * Delta_n)
  *   b_bar[n,:]   = (lambda_bar_n - 1) / lambda_n * b_tilde[n,:]
  * with the removable singularity lambda_n*Delta_n -> 0 taken as the limit
- * Delta_n * b_tilde[n,:].  Computed in float64 on the device and rounded once.
+ * Delta_n * b_tilde[n,:].  Computed on the device in float-float arithmetic
+ * (pairs of floats, ~48 significant bits, from FP32 instructions) and rounded
+ * once to float.  Launched with programmatic stream serialisation: it may
+ * start while the kernel before it runs, reads only its inputs until that
+ * kernel has completed, and writes lambda_bar and b_bar after.
  *   lambda     [P]    complex   in
  *   log_dt     [P]    float32   in
  *   b_tilde    [P,H]  complex   in
@@ -92,8 +96,8 @@ s5_status s5_discretize(const float *lambda, const float *log_dt, const float *b
  *           physical meaning"; summary section 6.2):
  *           Delta_n = dt_scale * exp(log_dt[n]) with dt_scale = old sampling
  *           rate / new sampling rate (16 kHz -> 8 kHz gives 2).  Must be > 0.
- * Computed in float64 on the device and rounded once.  Arrays as in
- * s5_discretize.  Errors: S5_ERR_INVALID_ARGUMENT for null/misaligned
+ * Computed in float-float arithmetic and rounded once, as s5_discretize.
+ * Arrays as in s5_discretize.  Errors: S5_ERR_INVALID_ARGUMENT for null/misaligned
  * pointers, P, H < 1, an unknown method, dt_scale <= 0 or clip_re > 0.
  */
 s5_status s5_discretize_ex(const float *lambda, const float *log_dt, const float *b_tilde, int P, int H,
