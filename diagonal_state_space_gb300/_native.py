@@ -40,6 +40,8 @@ SIGNATURES = {
     "s5_gate_residual": (_i, [_vp, _vp, _vp, _vp, _vp, _ll, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "s5_gate_backward": (_i, [_vp, _vp, _vp, _vp, _ll, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "s5_ssm_backward": (_i, [_vp] * 16 + [_i] * 4 + [_vp] * 7 + [_sz, _vp]),
+    "s5_gemm_bf16": (_i, [_i, _i, _i, _i, _i, _vp, _ll, _vp, _ll, _vp, _ll, _vp]),
+    "s5_gemm_fault": (_i, []),
 }
 
 _lock = threading.Lock()
@@ -82,4 +84,4 @@ def check(fn: str, code: int) -> None:
 
 
 STACK_FUNCTIONS = {"s5_layernorm", "s5_stack_weights", "s5_ssm_forward_states", "s5_gate_residual",
-                   "s5_gate_backward", "s5_ssm_backward"}
+                   "s5_gate_backward", "s5_ssm_backward", "s5_gemm_bf16"}

@@ -24,12 +24,7 @@ NVCC_FLAGS = [
     "-I", os.path.join(ROOT, "include"),
 ]
 
-
-# cuBLAS (the stack's plain bf16 GEMMs), found at run time through the
-# toolkit's library directory.
-_CUDA_LIB = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(
-    shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))), "lib64")
-LINK_LIBS = ["-L" + _CUDA_LIB, "-lcublas", "-Xlinker", "-rpath," + _CUDA_LIB]
+LINK_LIBS: list[str] = []
 
 
 def _nvcc() -> str:

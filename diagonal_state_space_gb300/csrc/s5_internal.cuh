@@ -10,6 +10,15 @@
 
 namespace s5 {
 
+// Row-major C[M][N] (fp32) = op(A) op(B) with bf16 operands: A is [M][K], or
+// [K][M] with ta; B is [K][N], or [N][K] with tb; row pitches in elements
+// (s5_gemm.cu).  Asynchronous on st.
+cudaError_t gemm_bf16(cudaStream_t st, bool ta, bool tb, int M, int N, int K, const void *A, long long lda,
+                      const void *B, long long ldb, float *C, long long ldc);
+// Reads and clears the flag set when a wait inside the GEMM kernel ran out
+// (1), 0 if none, -1 if the flag could not be read.
+int gemm_fault_take();
+
 // Records a CUDA error as the text s5_last_cuda_error() returns and gives
 // S5_ERR_CUDA (defined with the entry points in s5_api.cu).
 s5_status cuda_failure(cudaError_t e);

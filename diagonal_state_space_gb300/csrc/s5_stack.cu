@@ -18,10 +18,8 @@
 // Dense contractions (B_bar z, C' X, W h and the weight gradients) are plain
 // bf16 GEMMs with fp32 accumulation, run by cuBLAS; every other step is a
 // kernel of this file.  Scans are complex fp32.
-#include <cublas_v2.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "s5_internal.cuh"
 
@@ -733,28 +731,12 @@ __global__ void dc_finish_kernel(const float *__restrict__ g, int H, int P, floa
 }
 
 // ---------------------------------------------------------------------------
-// cuBLAS: one handle per device, used under a lock (the stream is set per call).
 // Row-major C[M][N] = op(A) op(B) with bf16 operands, fp32 accumulation and
-// output: column-major cuBLAS computes C^T = op(B)^T op(A)^T.
+// output: the tensor-core GEMM of s5_gemm.cu.
 // ---------------------------------------------------------------------------
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {nullptr};
-
-cublasStatus_t gemm_rm(cudaStream_t st, bool ta, bool tb, int M, int N, int K, const void *A, int lda,
-                       const void *B, int ldb, float *C, int ldc, float alpha = 1.f, float beta = 0.f) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CUBLAS_STATUS_NOT_INITIALIZED;
-    std::lock_guard<std::mutex> lk(g_blas_mu);
-    if (!g_blas[dev]) {
-        cublasStatus_t s = cublasCreate(&g_blas[dev]);
-        if (s != CUBLAS_STATUS_SUCCESS) return s;
-    }
-    cublasHandle_t h = g_blas[dev];
-    cublasStatus_t s = cublasSetStream(h, st);
-    if (s != CUBLAS_STATUS_SUCCESS) return s;
-    return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K, &alpha, B,
-                        CUDA_R_16BF, ldb, A, CUDA_R_16BF, lda, &beta, C, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F,
-                        CUBLAS_GEMM_DEFAULT);
+cudaError_t gemm_rm(cudaStream_t st, bool ta, bool tb, int M, int N, int K, const void *A, int lda,
+                    const void *B, int ldb, float *C, int ldc) {
+    return gemm_bf16(st, ta, tb, M, N, K, A, lda, B, ldb, C, ldc);
 }
 
 int grid_for(long long n, int threads) {
@@ -822,18 +804,27 @@ s5_status cuda_status(cudaError_t e) {
     std::snprintf(g_err, sizeof(g_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
     return S5_ERR_CUDA;
 }
-s5_status blas_status(cublasStatus_t s) {
-    if (s == CUBLAS_STATUS_SUCCESS) return S5_OK;
-    std::snprintf(g_err, sizeof(g_err), "cuBLAS status %d", (int)s);
-    return S5_ERR_CUDA;
-}
 #define S5_TRY_CUDA(x) do { s5_status s_ = cuda_status(x); if (s_ != S5_OK) return s_; } while (0)
-#define S5_TRY_BLAS(x) do { s5_status s_ = blas_status(x); if (s_ != S5_OK) return s_; } while (0)
 }  // namespace
 
 extern "C" {
 
 const char *s5_stack_last_error(void) { return g_err; }
+
+s5_status s5_gemm_bf16(int ta, int tb, int M, int N, int K, const void *A, long long lda, const void *B,
+                       long long ldb, float *C, long long ldc, s5_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return S5_ERR_INVALID_ARGUMENT;
+    if (M == 0 || N == 0) return S5_OK;
+    if (!C || ldc < N || (K > 0 && (!A || !B))) return S5_ERR_INVALID_ARGUMENT;
+    if (K > 0 && (lda < (ta ? M : K) || ldb < (tb ? K : N))) return S5_ERR_INVALID_ARGUMENT;
+    return cuda_status(s5::gemm_bf16(reinterpret_cast<cudaStream_t>(stream), ta != 0, tb != 0, M, N, K, A, lda, B,
+                                     ldb, C, ldc));
+}
+
+int s5_gemm_fault(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    return s5::gemm_fault_take();
+}
 
 size_t s5_stack_workspace_size(int B, int L, int H, int P) {
     if (B < 1 || L < 1 || H < 1 || P < 1) return 0;
@@ -890,7 +881,7 @@ s5_status s5_ssm_forward_states(const float *lambda_bar, const void *bs, const v
     s5::stack_ws_layout(T, B, H, P, workspace, &w);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // Bu [T][2P] = z16 [T][H] bs^T
-    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)T, 2 * P, H, z_bf16, H, bs, H, w.fa, 2 * P));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, true, (int)T, 2 * P, H, z_bf16, H, bs, H, w.fa, 2 * P));
     const int NC = (L + s5::SCAN_CL - 1) / s5::SCAN_CL;
     dim3 grid((P + s5::SCAN_THREADS - 1) / s5::SCAN_THREADS, NC, B);
     s5::scan_agg_fwd_kernel<<<grid, s5::SCAN_THREADS, 0, st>>>(w.fa, reinterpret_cast<const float2 *>(lambda_bar),
@@ -901,7 +892,7 @@ s5_status s5_ssm_forward_states(const float *lambda_bar, const void *bs, const v
         reinterpret_cast<float2 *>(x), static_cast<__nv_bfloat162 *>(X));
     S5_TRY_CUDA(cudaGetLastError());
     // y [T][H] = X [T][2P] cp^T  (the D term is added by the gate's first pass)
-    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)T, H, 2 * P, X, 2 * P, cp, 2 * P, y, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, true, (int)T, H, 2 * P, X, 2 * P, cp, 2 * P, y, H));
     return S5_OK;
 }
 
@@ -920,7 +911,7 @@ s5_status s5_gate_residual(const float *y_ssm, const float *z, const float *d, c
     s5::gate_pre_kernel<<<s5::grid_for((n + 3) / 4, 256), 256, 0, st>>>(y_ssm, z, d, y, h16, n, H);
     S5_TRY_CUDA(cudaGetLastError());
     // a [N][H] = h [N][H] W^T
-    S5_TRY_BLAS(s5::gemm_rm(st, false, true, (int)N, H, H, h16, H, w16, H, a, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, true, (int)N, H, H, h16, H, w16, H, a, H));
     s5::gate_post_kernel<<<s5::grid_for((n + 3) / 4, 256), 256, 0, st>>>(u, y, a, u_next, n);
     return cuda_status(cudaGetLastError());
 }
@@ -945,9 +936,9 @@ s5_status s5_gate_backward(const float *ubar, const float *y, const float *a, co
     s5::gate_bwd_pre_kernel<<<s5::grid_for((n + 3) / 4, 256), 256, 0, st>>>(ubar, y, a, act16, ydir, h16, n);
     S5_TRY_CUDA(cudaGetLastError());
     // W^T act: row-major [N][H] = act [N][H] W [H][H]
-    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)N, H, H, act16, H, w16, H, wact, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, false, (int)N, H, H, act16, H, w16, H, wact, H));
     // dW [H][H] = act^T h
-    S5_TRY_BLAS(s5::gemm_rm(st, true, false, H, H, (int)N, act16, H, h16, H, dW, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, true, false, H, H, (int)N, act16, H, h16, H, dW, H));
     s5::gate_bwd_post_kernel<<<s5::grid_for((n + 3) / 4, 256), 256, 0, st>>>(ydir, wact, y, ybar,
                                                                     static_cast<__nv_bfloat16 *>(ybar_bf16), n);
     return cuda_status(cudaGetLastError());
@@ -974,7 +965,7 @@ s5_status s5_ssm_backward(const float *lambda, const float *log_dt, const float 
     s5::stack_ws_layout(T, B, H, P, workspace, &w);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // x_hat [T][2P] = ybar16 [T][H] cx [H][2P]
-    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)T, 2 * P, H, ybar_bf16, H, cx, 2 * P, w.fa, 2 * P));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, false, (int)T, 2 * P, H, ybar_bf16, H, cx, 2 * P, w.fa, 2 * P));
     const int NC = (L + s5::SCAN_CL - 1) / s5::SCAN_CL;
     dim3 grid((P + s5::SCAN_THREADS - 1) / s5::SCAN_THREADS, NC, B);
     s5::scan_agg_bwd_kernel<<<grid, s5::SCAN_THREADS, 0, st>>>(w.fa, reinterpret_cast<const float2 *>(lambda_bar),
@@ -985,11 +976,11 @@ s5_status s5_ssm_backward(const float *lambda, const float *log_dt, const float 
         reinterpret_cast<const float2 *>(x0), w.agg, L, P, NC, w.c16, w.dlam);
     S5_TRY_CUDA(cudaGetLastError());
     // Re(B_bar^H s) [T][H] = S16 [T][2P] bs [2P][H]
-    S5_TRY_BLAS(s5::gemm_rm(st, false, false, (int)T, H, 2 * P, w.c16, 2 * P, bs, H, w.fb, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, false, false, (int)T, H, 2 * P, w.c16, 2 * P, bs, H, w.fb, H));
     // dB_bar [2P][H] = S16^T z16
-    S5_TRY_BLAS(s5::gemm_rm(st, true, false, 2 * P, H, (int)T, w.c16, 2 * P, z_bf16, H, w.dbbar, H));
+    S5_TRY_CUDA(s5::gemm_rm(st, true, false, 2 * P, H, (int)T, w.c16, 2 * P, z_bf16, H, w.dbbar, H));
     // G [H][2P] = ybar16^T X
-    S5_TRY_BLAS(s5::gemm_rm(st, true, false, H, 2 * P, (int)T, ybar_bf16, H, X, 2 * P, w.gdc, 2 * P));
+    S5_TRY_CUDA(s5::gemm_rm(st, true, false, H, 2 * P, (int)T, ybar_bf16, H, X, 2 * P, w.gdc, 2 * P));
     // LayerNorm backward (zbar = Re(B_bar^H s) + D ybar) and the residual; dD partials
     const size_t ln_smem = sizeof(float) * (s5::LNB_THREADS / 32) * H;
     if (H % 4 == 0 && H <= 128)

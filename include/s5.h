@@ -245,8 +245,8 @@ s5_status s5_forward_noalloc(const float *lambda_bar, const float *b_bar, const 
  * Shared conventions: device pointers owned by the caller, 16-byte aligned;
  * T = N = B*L tokens, row-major [T][H] activations; complex arrays are
  * interleaved (re, im) float pairs.  Dense contractions are bf16 GEMMs with
- * fp32 accumulation (cuBLAS); every other step runs in this library's
- * kernels.  Calls are asynchronous on `stream`; the return value reports
+ * fp32 accumulation on the tensor cores (s5_gemm_bf16 below); every step
+ * runs in this library's kernels.  Calls are asynchronous on `stream`; the return value reports
  * argument and launch errors (S5_ERR_CUDA: text in s5_stack_last_error()).
  * ======================================================================== */
 
@@ -255,8 +255,30 @@ s5_status s5_forward_noalloc(const float *lambda_bar, const float *b_bar, const 
  * initialisation and are scratch between calls. */
 size_t s5_stack_workspace_size(int B, int L, int H, int P);
 
-/* Text of the last CUDA or cuBLAS error of the stack entry points. */
+/* Text of the last CUDA error of the stack entry points. */
 const char *s5_stack_last_error(void);
+
+/* The stack's dense contraction (wiki "Method" step 4 and its pseudocode:
+ * B_bar z, the readout 2 Re(C~ x) over X, the gate's W h; review rows 1 and
+ * 4; and the adjoint products of the backward):
+ *   C[M][N] = op(A) op(B),  bf16 operands, fp32 accumulation and output.
+ * A is row-major [M][K] (lda >= K), or with ta != 0 [K][M] (lda >= M);
+ * B is row-major [K][N] (ldb >= N), or with tb != 0 [N][K] (ldb >= K);
+ * C is row-major [M][N], ldc >= N.  Pitches are in elements.  C is
+ * overwritten (no accumulation into it).  When the operand bases are
+ * 16-byte aligned and lda, ldb are multiples of 8 the product runs on the
+ * tensor cores (tcgen05, TMA-fed, K split over the SMs when the output is
+ * small and K long); other shapes run on a CUDA-core kernel.  M, N = 0 is a
+ * no-op; K = 0 writes zeros.  Asynchronous on `stream`.  Errors:
+ * S5_ERR_INVALID_ARGUMENT (negative sizes, null pointers, pitches too small),
+ * S5_ERR_CUDA (launch; text in s5_stack_last_error()). */
+s5_status s5_gemm_bf16(int ta, int tb, int M, int N, int K, const void *A, long long lda, const void *B,
+                       long long ldb, float *C, long long ldc, s5_stream_t stream);
+
+/* 1 if a wait inside the tensor-core GEMM ran out since the last call (the
+ * products of that launch are then not valid), 0 if none; the flag is
+ * cleared.  Synchronises the device. */
+int s5_gemm_fault(void);
 
 /* LayerNorm over the last axis without affine parameters, biased variance,
  * eps = 1e-5:  z = (x - mean(x)) / sqrt(var(x) + eps) per row.

@@ -102,3 +102,17 @@ def test_host_validation_of_the_next_row_entry_points(lib):
     assert lib.s5_forward_bidirectional(*bad) == INV
     bad = list(bargs); bad[10] = 0                     # L = 0: nothing to do
     assert lib.s5_forward_bidirectional(*bad) == OK
+
+
+def test_host_validation_of_the_gemm(lib):
+    INV = 1
+    fake = ctypes.c_void_p(1 << 20)
+    # negative sizes, missing operands, pitches below the row length
+    assert lib.s5_gemm_bf16(0, 0, -1, 4, 4, fake, 4, fake, 4, fake, 4, None) == INV
+    assert lib.s5_gemm_bf16(0, 0, 4, 4, 4, None, 4, fake, 4, fake, 4, None) == INV
+    assert lib.s5_gemm_bf16(0, 0, 4, 4, 8, fake, 4, fake, 4, fake, 4, None) == INV   # lda < K
+    assert lib.s5_gemm_bf16(1, 0, 8, 4, 4, fake, 4, fake, 4, fake, 4, None) == INV   # ta: lda < M
+    assert lib.s5_gemm_bf16(0, 1, 4, 4, 8, fake, 8, fake, 4, fake, 4, None) == INV   # tb: ldb < K
+    assert lib.s5_gemm_bf16(0, 0, 4, 8, 4, fake, 4, fake, 8, fake, 4, None) == INV   # ldc < N
+    # an empty product is a no-op that launches nothing
+    assert lib.s5_gemm_bf16(0, 0, 0, 4, 4, None, 0, None, 0, None, 0, None) == 0
