@@ -765,6 +765,21 @@ def run_stack(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    # The K timed steps are captured once into a CUDA graph and replayed once
+    # between events (the step is ~140 launches; replaying them from a graph
+    # takes the host's per-call work out of the timed region, as a training
+    # loop that captures its step would).  Eager timing if capture fails.
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                step()
+        graph.replay()   # one untimed replay: the graph's first launch uploads it
+        torch.cuda.synchronize()
+    except Exception as exc:  # noqa: BLE001
+        print("bench: stack graph capture failed (%s); timing eagerly" % exc, file=sys.stderr)
+        graph = None
     sampler = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -773,8 +788,11 @@ def run_stack(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
     e1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -852,6 +870,8 @@ def run_stack(args):
                    "global_batch": w.B * world, "seq_len": w.L,
                    "l2": "activations of %.1f GB per step, far above the 129 MB L2"
                          % (st.u.numel() * 4 * 7 / 1e9),
+                   "timing": ("K steps captured in one CUDA graph, replayed once between events"
+                              if graph is not None else "K steps launched eagerly between events"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": "whole step (bf16 GEMMs + scans + elementwise)",
                      "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s",

@@ -15,7 +15,7 @@
 //             M-elements 8 KB apart; a K-step of 16 advances the start by 2 KB
 //
 // Kernel: persistent, one CTA per SM, tiles of 128 x 256 (one M=128, N=256,
-// K=16 MMA per K-step), 64-deep K-blocks through a 3-stage ring.
+// K=16 MMA per K-step), 64-deep K-blocks through a 4-stage ring.
 //   warp 0      TMA producer (one elected thread)
 //   warp 1      TMEM allocation and MMA issue (one elected thread); two
 //               accumulators of 256 columns, so that the epilogue of a tile
@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "s5_internal.cuh"
 #include "s5_sm100.cuh"
@@ -46,7 +47,7 @@ using namespace sm100;
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int GSTAGES = 3;
+constexpr int GSTAGES = 4;
 constexpr int GTHREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
@@ -390,31 +391,58 @@ PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn() {
     return fn;
 }
 
-// 2-D bf16 map of a row-major [rows][cols] matrix with row pitch ld
-// elements; box {64 columns, box_rows rows}, 128-byte swizzle, zero fill.
-bool gemm_map(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld, int box_rows) {
-    auto fn = gemm_encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+// Encoded tensor maps are cached by what they encode: the stack calls the
+// same products on the same buffers every step, and encoding is host work.
+struct MapKey {
+    const void *base;
+    long long rows, cols, ld;
+    int box_rows, dtype;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && box_rows == o.box_rows &&
+               dtype == o.dtype;
+    }
+};
+constexpr int MAP_CACHE = 256;
+std::mutex g_map_mu;
+MapKey g_map_keys[MAP_CACHE];
+CUtensorMap g_map_vals[MAP_CACHE];
+int g_map_used = 0, g_map_next = 0;
 
-// 2-D fp32 map of C [rows][cols], pitch ld elements; box 32 x 32, 128-byte swizzle.
-bool gemm_map_c(CUtensorMap *map, float *base, long long rows, long long cols, long long ld) {
+// 2-D map of a row-major [rows][cols] matrix with row pitch ld elements; box
+// {box_cols columns, box_rows rows}, 128-byte swizzle, zero fill.  dtype 0:
+// bf16 (box_cols 64), 1: fp32 (box_cols 32).
+bool cached_map(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld, int box_rows,
+                int dtype) {
+    const MapKey key{base, rows, cols, ld, box_rows, dtype};
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+        if (g_map_keys[i] == key) {
+            *map = g_map_vals[i];
+            return true;
+        }
     auto fn = gemm_encode_fn();
     if (!fn) return false;
+    const bool f32 = dtype == 1;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * (f32 ? 4 : 2)};
+    cuuint32_t box[2] = {f32 ? 32u : 64u, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           f32 ? CU_TENSOR_MAP_L2_PROMOTION_NONE : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    const int slot = g_map_used < MAP_CACHE ? g_map_used++ : (g_map_next++ % MAP_CACHE);
+    g_map_keys[slot] = key;
+    g_map_vals[slot] = *map;
+    return true;
+}
+bool gemm_map(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld, int box_rows) {
+    return cached_map(map, base, rows, cols, ld, box_rows, 0);
+}
+// fp32 C [rows][cols], box 32 x 32
+bool gemm_map_c(CUtensorMap *map, float *base, long long rows, long long cols, long long ld) {
+    return cached_map(map, base, rows, cols, ld, 32, 1);
 }
 
 int g_num_sms[64] = {0};
