@@ -883,8 +883,9 @@ def run_stack(args):
                 "ms_per_step": e2e_ms},
         # per step one discretize of all layers' modes; per layer: forward weights,
         # LayerNorm, scan aggregates + apply, gate pre/post; backward gate pre/post,
-        # scan aggregates + apply, LayerNorm, dD sum, ZOH chain, dC~ (cuBLAS GEMMs not counted)
-        "gpu_launches": args.steps * (1 + w.layers * 14),
+        # scan aggregates + apply, LayerNorm, dD sum, ZOH chain, dC~; and the nine
+        # tensor-core GEMMs (three forward, six backward)
+        "gpu_launches": args.steps * (1 + w.layers * 23),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
