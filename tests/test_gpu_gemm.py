@@ -79,3 +79,24 @@ def test_gemm_k_zero_writes_zeros():
     _native.check("s5_gemm_bf16", code)
     torch.cuda.synchronize()
     assert torch.count_nonzero(C).item() == 0
+
+
+@pytest.mark.parametrize("K", [192, 8192])
+def test_gemm_output_pitch_tma_cannot_store(K):
+    # operands TMA can read, but an output pitch of N + 1 floats (not a
+    # multiple of 16 bytes): the tensor-core kernel writes C with per-thread
+    # stores (K = 8192 also splits K and adds the partial products atomically);
+    # the padding column stays untouched
+    rng = np.random.default_rng(K)
+    M, N = 256, 64
+    A, a = _operand(rng, M, K, K)
+    B, b = _operand(rng, N, K, K)
+    C = torch.full((M, N + 1), 7.0, dtype=torch.float32, device="cuda")
+    lib = _native.lib()
+    code = lib.s5_gemm_bf16(0, 1, M, N, K, A.data_ptr(), K, B.data_ptr(), K, C.data_ptr(), N + 1, None)
+    _native.check("s5_gemm_bf16", code)
+    torch.cuda.synchronize()
+    assert lib.s5_gemm_fault() == 0
+    got = C.cpu().numpy().astype(np.float64)
+    check(got[:, :N], a @ b.T, TOL, "C")
+    assert np.all(got[:, N] == 7.0)
