@@ -64,6 +64,7 @@ __device__ int g_gemm_fault = 0;   // a bounded wait ran out
 struct GemmBars {
     uint64_t full[GSTAGES], empty[GSTAGES];
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t drain;   // every MMA issued has completed (before TMEM is freed)
     uint32_t tmem_base;
     int abort;
 };
@@ -151,6 +152,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             mbar_init(&gb->acc_full[a], 1);
             mbar_init(&gb->acc_empty[a], 4);
         }
+        mbar_init(&gb->drain, 1);
         gb->abort = 0;
         fence_mbar_init();
     }
@@ -251,6 +253,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             if (elect_one()) mma_commit(&gb->acc_full[ab]);
             __syncwarp();
         }
+        // every MMA issued must complete before TMEM is freed (after a wait
+        // gave up, some may still be in flight): bounded wait on a last commit
+        if (elect_one()) mma_commit(&gb->drain);
+        __syncwarp();
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait_sleep(&gb->drain, 0, 1000000))
+            if (global_ns() - t0 > 200000000ull) break;
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;   // TMEM lane quarter of this warp
@@ -334,11 +343,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
-        // every MMA issued has completed once its accumulator was read, or
-        // (after an abort) once this commit arrives
-        tmem_dealloc(tmem, 512);
-    }
+    if (warp == 1) tmem_dealloc(tmem, 512);   // the MMA warp drained its MMAs above
 }
 
 // Plain CUDA-core GEMM for shapes TMA cannot address: 32 x 32 output tiles,
