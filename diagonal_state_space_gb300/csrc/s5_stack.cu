@@ -16,8 +16,8 @@
 // then the zero-order hold's chain rule to lambda, log_dt and B~.
 //
 // Dense contractions (B_bar z, C' X, W h and the weight gradients) are plain
-// bf16 GEMMs with fp32 accumulation, run by cuBLAS; every other step is a
-// kernel of this file.  Scans are complex fp32.
+// bf16 GEMMs with fp32 accumulation on the tensor cores (s5_gemm.cu); every
+// other step is a kernel of this file.  Scans are complex fp32.
 
 #include <cstdio>
 
