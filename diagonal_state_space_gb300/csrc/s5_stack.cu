@@ -751,6 +751,9 @@ int grid_for(long long n, int threads) {
 //   f32 [T][max(2P, H)] x2 (A, Bf), bf16 [T][max(2P, H)] x2 (C16, D16),
 //   f32 [2P][H] (dB_bar), f32 [H][2P] (G of dC~), float2 [B][P] (dlambda_bar
 //   partials), f32 [LNB_BLOCKS][H] (dD partials)
+// D16 is not used by the SSM calls: with it the regions before dB_bar span at
+// least 12 T H bytes, the scratch s5_gate_backward takes from the same
+// workspace.
 constexpr int LNB_BLOCKS = 304;
 constexpr int LNB_THREADS = 256;
 
