@@ -732,10 +732,14 @@ STACK_METRIC = "S5 stack training step (fwd+bwd) tokens/s"
 
 def stack_flops(B, L, H, P, nl):
     """Dense flops of one forward + backward step (the bf16 GEMMs): per layer
-    forward Bu (2T*H*2P), readout (2T*2P*H), gate (2T*H*H); backward gate
-    (two of 2T*H*H), x_hat, zbar, dB_bar, dC~ (four of 2T*H*2P)."""
+    forward Bu and the readout (two of 2T*H*2P) and the gate's W h (2T*H*H);
+    backward W^T act and dW (two of 2T*H*H) and x_hat, zbar, dB_bar, dC~
+    (four of 2T*H*2P): nine products."""
     T = B * L
-    return nl * (3 * 2 * T * H * 2 * P + 3 * 2 * T * H * H + 4 * 2 * T * H * 2 * P)
+    mode_gemm, gate_gemm = 2 * T * H * 2 * P, 2 * T * H * H
+    forward = 2 * mode_gemm + gate_gemm
+    backward = 4 * mode_gemm + 2 * gate_gemm
+    return nl * (forward + backward)
 
 
 def run_stack(args):

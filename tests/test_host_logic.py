@@ -70,6 +70,28 @@ def test_algorithmic_bytes_of_the_long_sequence_workload():
     assert bench.algorithmic_bytes(wb, 2, 2) == expect + 8 * 128 * 128
 
 
+def test_stack_flops_count_the_nine_products_of_a_layer():
+    import bench
+
+    B, L, H, P, nl = 32, 1024, 512, 256, 6
+    T = B * L
+    # (M, N, K) of every product one layer issues (s5_ssm_forward_states,
+    # s5_gate_residual, s5_gate_backward, s5_ssm_backward)
+    products = [(T, 2 * P, H),   # Bu = z B_bar^T
+                (T, H, 2 * P),   # y = X C'^T
+                (T, H, H),       # a = h W^T
+                (T, H, H),       # W^T act
+                (H, H, T),       # dW = act^T h
+                (T, 2 * P, H),   # x_hat = ybar C'
+                (T, H, 2 * P),   # Re(B_bar^H s)
+                (2 * P, H, T),   # dB_bar = S^T z
+                (H, 2 * P, T)]   # G = ybar^T X (dC~)
+    assert bench.stack_flops(B, L, H, P, nl) == nl * sum(2 * m * n * k for m, n, k in products)
+    assert bench.stack_flops(B, L, H, P, nl) == 927712935936
+    # a shape with 2P != H keeps the two kinds apart
+    assert bench.stack_flops(2, 77, 64, 48, 1) == 2 * 154 * (6 * 64 * 96 + 3 * 64 * 64)
+
+
 def test_reference_arm_prints_one_contract_line():
     # the float64 oracle on the host: no GPU is involved
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
